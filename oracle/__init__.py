@@ -1,0 +1,8 @@
+"""CPU float64 oracle for exact attention (test infrastructure only).
+
+Only the tests, the package smoke check and the bench's CPU-baseline leg import
+this package. The library never does.
+"""
+from .attention import (allowed_mask, head_forward, head_backward, attention_fwd,
+                        attention_fwd_bwd, tile_states, SKIP, FULL, PARTIAL, TILE)
+from .loops import loop_attention_fwd_bwd
