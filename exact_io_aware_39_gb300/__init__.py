@@ -1,0 +1,18 @@
+"""Exact, IO-aware attention (forward and backward) for NVIDIA GB300.
+
+The computation lives in libflashattn.so (hand-written sm_103a CUDA behind the
+C ABI of include/flash_attn.h); this package holds its ctypes binding, the
+in-place build script, the seeded synthetic inputs and FLOP accounting.
+Importing the package does not load the library; the first call does, and
+raises if it is missing.
+"""
+from ._lib import (FlashAttnError, attention_bwd, attention_fwd, device_error,
+                   flash_attn_bwd, flash_attn_bwd_workspace_size, flash_attn_fwd,
+                   flash_attn_get_device_error, flash_attn_status_string, flash_attn_tile_map,
+                   flash_attn_version, load, tile_map)
+
+__all__ = [
+    "FlashAttnError", "attention_bwd", "attention_fwd", "device_error", "flash_attn_bwd",
+    "flash_attn_bwd_workspace_size", "flash_attn_fwd", "flash_attn_get_device_error",
+    "flash_attn_status_string", "flash_attn_tile_map", "flash_attn_version", "load", "tile_map",
+]

@@ -1,0 +1,190 @@
+"""ctypes binding of libflashattn.so: the C ABI of include/flash_attn.h under
+the same names, plus thin helpers that take torch tensors.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI. There is no CPU or PyTorch fallback; if the shared
+library is missing or does not load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libflashattn.so")
+
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
+    4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_DEVICE_INTERNAL",
+}
+
+# every symbol include/flash_attn.h declares
+EXPORTS = [
+    "flash_attn_fwd", "flash_attn_bwd_workspace_size", "flash_attn_bwd", "flash_attn_tile_map",
+    "flash_attn_get_device_error", "flash_attn_status_string", "flash_attn_version",
+]
+
+
+class FlashAttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Loads (once) and returns the ctypes handle of the library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m exact_io_aware_39_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.flash_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, vp]
+    lib.flash_attn_fwd.restype = i32
+    lib.flash_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.flash_attn_bwd_workspace_size.restype = sz
+    lib.flash_attn_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]
+    lib.flash_attn_bwd.restype = i32
+    lib.flash_attn_tile_map.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.flash_attn_tile_map.restype = i32
+    lib.flash_attn_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.flash_attn_get_device_error.restype = i32
+    lib.flash_attn_status_string.argtypes = [i32]
+    lib.flash_attn_status_string.restype = ctypes.c_char_p
+    lib.flash_attn_version.argtypes = []
+    lib.flash_attn_version.restype = i32
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# raw C-ABI calls (same names and argument order as the header)
+# ---------------------------------------------------------------------------
+
+def flash_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, stream):
+    return load().flash_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, stream)
+
+
+def flash_attn_bwd_workspace_size(B, H, N, d):
+    return load().flash_attn_bwd_workspace_size(B, H, N, d)
+
+
+def flash_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, block_mask,
+                   workspace, workspace_bytes, stream):
+    return load().flash_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len,
+                                 block_mask, workspace, workspace_bytes, stream)
+
+
+def flash_attn_tile_map(B, N, causal, kv_len, block_mask, out, stream):
+    return load().flash_attn_tile_map(B, N, causal, kv_len, block_mask, out, stream)
+
+
+def flash_attn_get_device_error():
+    detail = (ctypes.c_uint32 * 4)()
+    st = load().flash_attn_get_device_error(detail)
+    return st, list(detail)
+
+
+def flash_attn_status_string(status):
+    return load().flash_attn_status_string(status).decode()
+
+
+def flash_attn_version():
+    return load().flash_attn_version()
+
+
+# ---------------------------------------------------------------------------
+# torch helpers (device memory and streams come from PyTorch)
+# ---------------------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st, where):
+    if st != FA_OK:
+        raise FlashAttnError(st, where)
+
+
+def _check_inputs(*ts):
+    import torch
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    for t in ts[:3]:
+        if t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("Q, K, V must be bfloat16 [B, H, N, d]")
+
+
+def _mask_args(kv_len, block_mask):
+    import torch
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor [B]")
+    if block_mask is not None and (block_mask.dtype != torch.uint8 or not block_mask.is_cuda):
+        raise ValueError("block_mask must be a CUDA uint8 tensor [nT, nT]")
+    return _ptr(kv_len), _ptr(block_mask)
+
+
+def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, out=None, lse=None,
+                  stream=None):
+    """O, LSE = attention(q, k, v) on the GPU. q, k, v: bf16 [B, H, N, d]."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    kv_p, bm_p = _mask_args(kv_len, block_mask)
+    st = flash_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, float(scale),
+                        int(bool(causal)), kv_p, bm_p, _stream(stream))
+    _check(st, "flash_attn_fwd")
+    return o, l
+
+
+def attention_bwd(q, k, v, o, do, lse, scale, causal=False, kv_len=None, block_mask=None,
+                  workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of attention on the GPU (recomputing S and P on chip)."""
+    import torch
+    _check_inputs(q, k, v, o, do)
+    B, H, N, d = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = flash_attn_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    kv_p, bm_p = _mask_args(kv_len, block_mask)
+    st = flash_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                        _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), kv_p, bm_p,
+                        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "flash_attn_bwd")
+    return dq, dk, dv
+
+
+def tile_map(B, N, causal=False, kv_len=None, block_mask=None, device="cuda", stream=None):
+    """uint8 [B, nT, nT] tile states the kernels use (0 skip, 1 full, 2 partial)."""
+    import torch
+    nT = (N + 127) // 128
+    out = torch.empty((B, nT, nT), dtype=torch.uint8, device=device)
+    kv_p, bm_p = _mask_args(kv_len, block_mask)
+    st = flash_attn_tile_map(B, N, int(bool(causal)), kv_p, bm_p, _ptr(out), _stream(stream))
+    _check(st, "flash_attn_tile_map")
+    return out
+
+
+def device_error():
+    """(status, [code, site, block, thread]) of the device error word; clears it."""
+    return flash_attn_get_device_error()

@@ -1,0 +1,244 @@
+// C ABI of the attention library: argument validation, TMA tensor-map
+// construction, launches, the tile classifier export and the device error
+// word. Declarations and the contract of every call are in flash_attn.h.
+#include "flash_attn.h"
+#include "fa_common.cuh"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+namespace fa {
+
+// Device error word: {code, site, block, thread}. One copy per device that
+// loads the library; kernels receive its address.
+__device__ unsigned int g_fa_err[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: checks for a compute capability 10.3 device and looks up
+// the address of the error word on it.
+fa_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_fa_err) != cudaSuccess) return FA_ERR_CUDA;
+      st.err = static_cast<unsigned int*>(p);
+    }
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  if (!st.supported) return FA_ERR_UNSUPPORTED;
+  *out = &st;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D view [BH, N, d] of a bf16 tensor, box 64 x 128 x 1, 128-byte swizzle;
+// rows past N read as zeros and are not written by stores.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status check_shape(int B, int H, int N, int d, float scale, int causal) {
+  if (B < 1 || H < 1 || N < 1 || !std::isfinite(scale) || (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (N > kMaxN) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  const long long nT = (N + kTile - 1) / kTile;
+  if (BH * nT > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+__global__ void tile_map_kernel(int B, int N, int nT, int causal, const int32_t* kv_len, const uint8_t* bm,
+                                uint8_t* out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)B * nT * nT;
+  if (idx >= total) return;
+  const int b = (int)(idx / ((long long)nT * nT));
+  const int rem = (int)(idx % ((long long)nT * nT));
+  const int qi = rem / nT, kj = rem % nT;
+  out[idx] = (uint8_t)tile_state(qi, kj, effective_kv_len(kv_len, b, N), nT, causal, bm);
+}
+
+}  // namespace
+
+cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len, const uint8_t* block_mask,
+                            uint8_t* out, cudaStream_t s) {
+  const long long total = (long long)B * nT * nT;
+  const unsigned grid = (unsigned)((total + 255) / 256);
+  tile_map_kernel<<<grid, 256, 0, s>>>(B, N, nT, causal, kv_len, block_mask, out);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                         int d, float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
+                         void* stream) {
+  fa_status st = check_shape(B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return FA_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (make_map(&tq, Q, BH, N, d) || make_map(&tk, K, BH, N, d) || make_map(&tv, V, BH, N, d) ||
+      make_map(&to, O, BH, N, d))
+    return FA_ERR_CUDA;
+  FwdParams p{};
+  p.lse = LSE;
+  p.kv_len = kv_len;
+  p.block_mask = block_mask;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.nT = (N + kTile - 1) / kTile;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                             : FA_ERR_CUDA;
+}
+
+size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, 1.0f, 0) != FA_OK) return 0;
+  return bwd_workspace_layout(B, H, N, d).total;
+}
+
+fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                         const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                         int causal, const int32_t* kv_len, const uint8_t* block_mask, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  fa_status st = check_shape(B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
+  const BwdWorkspace w = bwd_workspace_layout(B, H, N, d);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  const int BH = B * H;
+  const int nT = (N + kTile - 1) / kTile;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  float* delta = reinterpret_cast<float*>(ws + w.delta_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (make_map(&tq, Q, BH, N, d) || make_map(&tk, K, BH, N, d) || make_map(&tv, V, BH, N, d) ||
+      make_map(&tdo, dO, BH, N, d) || make_map(&tdk, dK, BH, N, d) || make_map(&tdv, dV, BH, N, d))
+    return FA_ERR_CUDA;
+  if (launch_bwd_pre(O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  BwdParams p{};
+  p.kv_len = kv_len;
+  p.block_mask = block_mask;
+  p.dq_acc = dq_acc;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.nT = nT;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_dq(dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status flash_attn_tile_map(int B, int N, int causal, const int32_t* kv_len, const uint8_t* block_mask,
+                              uint8_t* out, void* stream) {
+  if (B < 1 || N < 1 || N > kMaxN || (causal != 0 && causal != 1) || out == nullptr) return FA_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  fa_status st = device_state(&ds);
+  if (st != FA_OK) return st;
+  const int nT = (N + kTile - 1) / kTile;
+  return launch_tile_map(B, N, nT, causal, kv_len, block_mask, out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status flash_attn_get_device_error(uint32_t* detail) {
+  DeviceState* ds = nullptr;
+  fa_status st = device_state(&ds);
+  if (st != FA_OK) return st;
+  unsigned int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, ds->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(ds->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  if (detail) std::memcpy(detail, h, sizeof(h));
+  if (h[0] == 0) return FA_OK;
+  if (h[0] == kErrTimeout) return FA_ERR_DEVICE_TIMEOUT;
+  return FA_ERR_DEVICE_INTERNAL;
+}
+
+const char* flash_attn_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE_INTERNAL: return "device internal error";
+  }
+  return "unknown status";
+}
+
+int flash_attn_version(void) { return 100; }
+
+}  // extern "C"

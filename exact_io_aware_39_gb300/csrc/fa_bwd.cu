@@ -1,0 +1,521 @@
+// Backward pass of exact attention by recomputation, for sm_103a.
+//
+// The method (FlashAttention milestone page (nlp-lineage), "The idea --
+// Recomputation"; FlashAttention proof-of-work page, "Activation Gradient
+// Recomputation"; pixelation.org article, "The Recomputation Trade-off"): keep
+// only O and the per-row softmax statistics from the forward pass and
+// recompute the attention blocks on chip, never storing the N x N matrix.
+// The gradient algebra is the textbook one for L = sum(dO * O):
+//   P = exp(scale * Q K^T - LSE), dV = P^T dO, dP = dO V^T,
+//   D = rowsum(dO * O), dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+//
+// Three launches on one stream:
+//   1. fa_bwd_pre:  D = rowsum(dO * O) in fp32, LSE2 = LSE * log2(e) (+inf on
+//      rows past N and on fully masked rows), dQ accumulator zeroed;
+//   2. fa_bwd_main: one CTA per (batch, head, 128-key tile), looping over the
+//      live 128-query tiles. TMEM holds dV and dK (accumulated over the whole
+//      loop), S^T, then P^T as packed bf16 in place, and dP^T, which is then
+//      reused for the dQ partial of the tile. Five tcgen05 MMAs per tile pair:
+//        S^T  = K Q^T          (A = K, B = Q,   both K-major)
+//        dP^T = V dO^T         (A = V, B = dO,  both K-major)
+//        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
+//        dK  += dS^T Q         (A = dS^T from smem K-major, B = Q MN-major)
+//        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
+//      dQ partials are added into an fp32 workspace with vector reductions.
+//      Warps: 0-3 recompute P and dS (thread = key row), 4-7 drain dQ from
+//      TMEM into the workspace (thread = query row), 8 TMA producer, 9 MMA.
+//   3. fa_bwd_dq:   dQ = bf16(scale * dQ_acc).
+#include "fa_common.cuh"
+#include "fa_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace fa {
+
+namespace {
+
+constexpr int kBwdThreads = 320;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kHalves = D / 64;
+  static constexpr int kStages = 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ = kV + kTileBytes;                  // [stages]
+  static constexpr int kdO = kQ + kStages * kTileBytes;       // [stages]
+  static constexpr int kdS = kdO + kStages * kTileBytes;      // 128 x 128 bf16
+  static constexpr int kRow = kdS + kTile * kTile * 2;        // [stages] x (LSE2[128], D[128])
+  static constexpr int kBar = kRow + kStages * 2 * kTile * 4;
+  static constexpr int bKV = 0;
+  static constexpr int bQFull = 1;
+  static constexpr int bQEmpty = bQFull + kStages;
+  static constexpr int bSFull = bQEmpty + kStages;
+  static constexpr int bPFull = bSFull + 1;
+  static constexpr int bdPFull = bPFull + 1;
+  static constexpr int bdSFull = bdPFull + 1;
+  static constexpr int bdSEmpty = bdSFull + 1;
+  static constexpr int bdQFull = bdSEmpty + 1;
+  static constexpr int bdQFree = bdQFull + 1;
+  static constexpr int bFinal = bdQFree + 1;
+  static constexpr int bDrain = bFinal + 1;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBar + 8 * kNumBars;
+  static constexpr int kSmemBytes = kMisc + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t swz_off(int r, int col) {
+  // byte offset of bf16 element (row r, column col) in a 128-row tile stored
+  // as 64-column halves 16 KB apart with 128-byte swizzling
+  const int h = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return (uint32_t)(h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4) + ((col & 7) << 1));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
+                   const BwdParams p, const float scale) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int BH = p.B * p.H;
+  const int Np = p.nT * kTile;
+  const int kj = blockIdx.x / BH;          // low key tiles (most live query tiles) first
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.H;
+  const int kvl = effective_kv_len(p.kv_len, b, p.N);
+
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  // live query tiles of this key tile, visited in ascending order by every role
+  auto next_live = [&](int i) -> int {
+    while (i < p.nT && tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) == kSkip) ++i;
+    return i;
+  };
+  Ctl ctl{p.err, abort_flag};
+
+  if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
+    if (tid == 0) {
+      uint32_t dummy = 0;
+      Ctl c0{p.err, &dummy};
+      report_error(c0, kErrSmemAlign, 100);
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < L::kNumBars; ++i)
+      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdQFree) ? 128u : 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(misc), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    int count = 0;
+    for (int i = 0; i < p.nT; ++i) count += tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) != kSkip;
+    misc[2] = (uint32_t)count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = misc[0];
+  const int len = (int)misc[2];
+  const uint32_t tdV = tmem;
+  const uint32_t tdK = tmem + (uint32_t)D;
+  const uint32_t tS = tmem + 2u * D;
+  const uint32_t tP = tmem + 2u * D + 128u;   // dP^T, then the dQ partial
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tq);
+      tma_prefetch_map(&tk);
+      tma_prefetch_map(&tv);
+      tma_prefetch_map(&tdo);
+      mbar_arrive_expect_tx(bar(L::bKV), 2u * L::kTileBytes);
+      for (int h = 0; h < L::kHalves; ++h) {
+        tma_load_3d(sbase + L::kK + h * 16384, &tk, bar(L::bKV), 64 * h, kTile * kj, bh);
+        tma_load_3d(sbase + L::kV + h * 16384, &tv, bar(L::bKV), 64 * h, kTile * kj, bh);
+      }
+      int nq = 0;
+      int i = next_live(0);
+      for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
+        const int s = it % L::kStages;
+        const uint32_t n = (uint32_t)(it / L::kStages);
+        if (it >= L::kStages && !mbar_wait(bar(L::bQEmpty + s), (n - 1) & 1u, ctl, 101)) break;
+        mbar_arrive_expect_tx(bar(L::bQFull + s), 2u * L::kTileBytes + 2u * kTile * 4u);
+        for (int h = 0; h < L::kHalves; ++h) {
+          tma_load_3d(sbase + L::kQ + s * L::kTileBytes + h * 16384, &tq, bar(L::bQFull + s),
+                      64 * h, kTile * i, bh);
+          tma_load_3d(sbase + L::kdO + s * L::kTileBytes + h * 16384, &tdo, bar(L::bQFull + s),
+                      64 * h, kTile * i, bh);
+        }
+        const size_t roff = (size_t)bh * Np + (size_t)kTile * i;
+        bulk_load(sbase + L::kRow + s * 1024, p.lse2 + roff, kTile * 4, bar(L::bQFull + s));
+        bulk_load(sbase + L::kRow + s * 1024 + 512, p.delta + roff, kTile * 4, bar(L::bQFull + s));
+        ++nq;
+      }
+      drain_wait(bar(L::bKV), 0);
+      for (int s = 0; s < L::kStages; ++s)
+        if (s < nq)
+          drain_wait(bar(L::bQFull + s),
+                     (uint32_t)((s + ((nq - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && len > 0) {
+      constexpr uint32_t idSP = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idK = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idQ = idesc_bf16(128, D, true, true);
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdS = sbase + L::kdS;
+      bool ok = mbar_wait(bar(L::bKV), 0, ctl, 110) && mbar_wait(bar(L::bQFull), 0, ctl, 111);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sbase + L::kQ, ks), idSP, ks > 0 ? 1u : 0u);
+        mma_commit(bar(L::bSFull));
+      }
+      for (int it = 0; it < len && ok; ++it) {
+        const int s = it % L::kStages;
+        const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
+        const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
+        // dP^T = V dO^T (the dQ partial of the previous tile must have been read out)
+        if (it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tP, desc_kmajor(sV, ks), desc_kmajor(sdO, ks), idSP, ks > 0 ? 1u : 0u);
+        mma_commit(bar(L::bdPFull));
+        // dV += P^T dO
+        if (!(ok = mbar_wait(bar(L::bPFull), (uint32_t)it & 1u, ctl, 113))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ts(tdV, tS + (uint32_t)ks * 8u, desc_mnmajor(sdO, ks), idV, (it > 0 || ks > 0) ? 1u : 0u);
+        // next S^T, overlapping the dS computation of this tile
+        if (it + 1 < len) {
+          const int s1 = (it + 1) % L::kStages;
+          if (!(ok = mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114))) break;
+          tc_fence_after();
+          const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
+          mma_commit(bar(L::bSFull));
+        }
+        // dK += dS^T Q ; dQ_i = dS K
+        if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)it & 1u, ctl, 115))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tdK, desc_kmajor(sdS, ks), desc_mnmajor(sQ, ks), idK, (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tP, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
+        mma_commit(bar(L::bdQFull));
+        mma_commit(bar(L::bQEmpty + s));
+        mma_commit(bar(L::bdSEmpty));
+      }
+      mma_commit(bar(L::bFinal));
+      mma_commit(bar(L::bDrain));
+      drain_wait(bar(L::bDrain), 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P and dS (thread = key row)
+    const int r = tid;
+    const int krow = kTile * kj + r;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int i = next_live(0);
+    for (int it = 0; it < len && ok; ++it, i = next_live(i + 1)) {
+      const bool partial = tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) == kPartial;
+      const int s = it % L::kStages;
+      if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 120))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)it & 1u, ctl, 121))) break;
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024);
+      const float* dlt = lse2 + kTile;
+      float x[128];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(tS + lane_off + 0u, u0);
+        tmem_ld32(tS + lane_off + 32u, u1);
+        tmem_ld32(tS + lane_off + 64u, u2);
+        tmem_ld32(tS + lane_off + 96u, u3);
+        tmem_ld_wait(u0);
+        tmem_ld_wait(u1);
+        tmem_ld_wait(u2);
+        tmem_ld_wait(u3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(u0[c]);
+          x[32 + c] = __uint_as_float(u1[c]);
+          x[64 + c] = __uint_as_float(u2[c]);
+          x[96 + c] = __uint_as_float(u3[c]);
+        }
+      }
+      // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = ex2(fmaf(x[c], sl2, -lse2[c]));
+      if (partial) {
+        const int q0 = kTile * i;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if ((p.causal && krow > q0 + c) || krow >= kvl) x[c] = 0.f;
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[64 * hh + 2 * c], x[64 * hh + 2 * c + 1]);
+        tmem_st32(tS + lane_off + 32u * hh, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::bPFull));
+
+      // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> bf16 -> swizzled smem
+      if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)it & 1u, ctl, 122))) break;
+      if (it > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(it - 1) & 1u, ctl, 123))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tP + lane_off + 32u * cc, u);
+        tmem_ld_wait(u);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int c0 = 32 * cc + 2 * c;
+          const float d0 = x[c0] * (__uint_as_float(u[2 * c]) - dlt[c0]);
+          const float d1 = x[c0 + 1] * (__uint_as_float(u[2 * c + 1]) - dlt[c0 + 1]);
+          pk[c] = pack_bf16x2(d0, d1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint8_t* dst = smem + L::kdS + swz_off(r, 32 * cc + 8 * k);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(L::bdSFull));
+    }
+
+    // epilogue: dV and scale * dK for every key row of the tile (zeros when
+    // no query tile was live), staged in the K/V buffers and stored by TMA
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    ok = ok && mbar_wait_warp(bar(L::bKV), 0, ctl, 124);
+    const bool have = ok && len > 0 && mbar_wait_warp(bar(L::bFinal), 0, ctl, 125);
+    tc_fence_after();
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t tacc = (which == 0 ? tdV : tdK) + lane_off;
+      const float mul = (which == 0) ? 1.f : scale;
+      uint8_t* stage = smem + (which == 0 ? L::kV : L::kK);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (have) {
+          tmem_ld32(tacc + 32u * cc, u);
+          tmem_ld_wait(u);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) u[c] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (r == 0) {
+      for (int h = 0; h < L::kHalves; ++h) {
+        tma_store_3d(&tdv, sbase + L::kV + h * 16384, 64 * h, kTile * kj, bh);
+        tma_store_3d(&tdk, sbase + L::kK + h * 16384, 64 * h, kTile * kj, bh);
+      }
+      bulk_commit_group();
+      bulk_wait_group_all();
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain (thread = query row)
+    const int r = tid - 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    int i = next_live(0);
+    for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
+      if (!mbar_wait_warp(bar(L::bdQFull), (uint32_t)it & 1u, ctl, 130)) break;
+      tc_fence_after();
+      float* dst = p.dq_acc + ((size_t)bh * Np + (size_t)kTile * i + r) * D;
+      uint32_t u[D / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tP + lane_off + 32u * cc, u[cc]);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(u[cc]);
+      tc_fence_before();
+      mbar_arrive(bar(L::bdQFree));
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          red_add_v4(dst + 32 * cc + 4 * k, __uint_as_float(u[cc][4 * k]), __uint_as_float(u[cc][4 * k + 1]),
+                     __uint_as_float(u[cc][4 * k + 2]), __uint_as_float(u[cc][4 * k + 3]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO * O) (fp32), LSE2 = LSE * log2(e) with +inf for -inf and
+// padding rows, dQ accumulator zeroed. One group of d/8 threads per row, each
+// owning 8 consecutive columns.
+template <int D>
+__global__ void fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                  const float* __restrict__ lse, float* __restrict__ dq_acc,
+                                  float* __restrict__ lse2, float* __restrict__ delta, int BH, int N, int Np) {
+  constexpr int G = D / 8;   // threads per row
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gid / G;           // over BH * Np
+  const int part = (int)(gid % G);
+  if (row >= (long long)BH * Np) return;
+  const int bh = (int)(row / Np);
+  const int n = (int)(row % Np);
+  float acc = 0.f;
+  if (n < N) {
+    const size_t off = ((size_t)bh * N + n) * D + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 af = __bfloat1622float2(a2[k]);
+      const float2 gf = __bfloat1622float2(g2[k]);
+      acc = fmaf(af.x, gf.x, acc);
+      acc = fmaf(af.y, gf.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D + part * 8);
+  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (part == 0) {
+    delta[row] = acc;
+    float v = INFINITY;
+    if (n < N) {
+      const float l = lse[(size_t)bh * N + n];
+      v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+    }
+    lse2[row] = v;
+  }
+}
+
+template <int D>
+__global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, float scale,
+                                 int BH, int N, int Np) {
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one thread per 8 columns
+  const long long total = (long long)BH * N * (D / 8);
+  if (gid >= total) return;
+  const long long row = gid / (D / 8);
+  const int part = (int)(gid % (D / 8));
+  const int bh = (int)(row / N);
+  const int n = (int)(row % N);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Np + n) * D + part * 8);
+  const float4 a = src[0], c = src[1];
+  uint4 out;
+  out.x = pack_bf16x2(a.x * scale, a.y * scale);
+  out.y = pack_bf16x2(a.z * scale, a.w * scale);
+  out.z = pack_bf16x2(c.x * scale, c.y * scale);
+  out.w = pack_bf16x2(c.z * scale, c.w * scale);
+  *reinterpret_cast<uint4*>(dq + (size_t)row * D + part * 8) = out;
+}
+
+template <int D>
+cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                              const BwdParams& p, float scale, cudaStream_t s) {
+  using L = BwdLayout<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const dim3 grid((unsigned)(p.nT * p.B * p.H));
+  fa_bwd_main_kernel<D><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
+                           float* delta, int BH, int N, int nT, int d, cudaStream_t s) {
+  const int Np = nT * kTile;
+  const long long threads = (long long)BH * Np * (d / 8);
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  if (d == 64)
+    fa_bwd_pre_kernel<64><<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                static_cast<const __nv_bfloat16*>(dout), lse, dq_acc, lse2,
+                                                delta, BH, N, Np);
+  else
+    fa_bwd_pre_kernel<128><<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                 static_cast<const __nv_bfloat16*>(dout), lse, dq_acc, lse2,
+                                                 delta, BH, N, Np);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const BwdParams& p, cudaStream_t s) {
+  const float scale = p.scale_log2 / 1.4426950408889634f;
+  if (d == 64) return launch_bwd_main_d<64>(tq, tk, tv, tdo, tdk, tdv, p, scale, s);
+  return launch_bwd_main_d<128>(tq, tk, tv, tdo, tdk, tdv, p, scale, s);
+}
+
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
+                          cudaStream_t s) {
+  const int Np = nT * kTile;
+  const long long threads = (long long)BH * N * (d / 8);
+  if (threads == 0) return cudaSuccess;
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  if (d == 64)
+    fa_bwd_dq_kernel<64><<<grid, block, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, BH, N, Np);
+  else
+    fa_bwd_dq_kernel<128><<<grid, block, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, BH, N, Np);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,102 @@
+// Shared definitions of the attention kernels: tile size, the tile
+// classifier, kernel parameter blocks and the internal launcher interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kTile = 128;            // rows of a Q tile and of a K/V tile
+constexpr int kMaxN = 131072;         // longest supported sequence
+
+enum TileState : int { kSkip = 0, kFull = 1, kPartial = 2 };
+
+// Device error word layout: [0] = first error code (0 = none), [1] = site id,
+// [2] = blockIdx.x of the reporting CTA, [3] = threadIdx.x.
+enum DeviceErr : uint32_t { kErrNone = 0, kErrTimeout = 5, kErrSmemAlign = 6 };
+
+// State of the (query tile qi, key tile kj) pair. kvl is the effective key
+// length of the batch entry, already clamped to [0, N]; bm is the block mask
+// (nT x nT, row = query tile) or null. Masks combine by AND: a tile is skipped
+// when its block is masked off, when it lies above the diagonal under the
+// causal mask, or when all its keys are at or past kvl; it is partial when it
+// straddles the diagonal or the key limit (keys past N always count as
+// masked, so the ragged last key tile is partial), and full otherwise.
+__host__ __device__ __forceinline__ int tile_state(int qi, int kj, int kvl, int nT, int causal,
+                                                   const uint8_t* bm) {
+  if (bm != nullptr && bm[qi * nT + kj] == 0) return kSkip;
+  if (causal && kj > qi) return kSkip;
+  if (kj * kTile >= kvl) return kSkip;
+  if ((causal && kj == qi) || (kj + 1) * kTile > kvl) return kPartial;
+  return kFull;
+}
+
+__host__ __device__ __forceinline__ int effective_kv_len(const int32_t* kv_len, int b, int N) {
+  if (kv_len == nullptr) return N;
+  int v = kv_len[b];
+  return v < 0 ? 0 : (v > N ? N : v);
+}
+
+struct FwdParams {
+  float* lse;                 // [BH, N] fp32
+  const int32_t* kv_len;      // [B] or null
+  const uint8_t* block_mask;  // [nT, nT] or null
+  unsigned int* err;          // device error word
+  int B, H, N, nT;
+  int causal;
+  float scale_log2;           // scale * log2(e)
+};
+
+struct BwdParams {
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+  float* dq_acc;              // [BH, nT*128, d] fp32 workspace
+  const float* lse2;          // [BH, nT*128] fp32 workspace: LSE * log2(e), +inf on padding
+  const float* delta;         // [BH, nT*128] fp32 workspace: rowsum(dO * O)
+  unsigned int* err;
+  int B, H, N, nT;
+  int causal;
+  float scale_log2;
+};
+
+// Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1,
+// 128-byte swizzle. Return the cudaError_t of the launch.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
+
+cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* dq_acc,
+                           float* lse2, float* delta, int BH, int N, int nT, int d,
+                           cudaStream_t s);
+
+cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdParams& p,
+                            cudaStream_t s);
+
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
+                          cudaStream_t s);
+
+cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len,
+                            const uint8_t* block_mask, uint8_t* out, cudaStream_t s);
+
+// Workspace layout of the backward pass (byte offsets, 256-aligned sections).
+struct BwdWorkspace {
+  size_t dq_off, lse2_off, delta_off, total;
+};
+
+inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t BH = (size_t)B * H;
+  const size_t Np = (size_t)((N + kTile - 1) / kTile) * kTile;
+  BwdWorkspace w;
+  w.dq_off = 0;
+  w.lse2_off = al(w.dq_off + BH * Np * d * sizeof(float));
+  w.delta_off = al(w.lse2_off + BH * Np * sizeof(float));
+  w.total = al(w.delta_off + BH * Np * sizeof(float));
+  return w;
+}
+
+}  // namespace fa

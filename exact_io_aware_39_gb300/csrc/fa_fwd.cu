@@ -1,0 +1,446 @@
+// Forward pass of exact attention, tile by tile with online softmax, for
+// sm_103a (tcgen05 tensor cores, TMEM accumulators, TMA staging).
+//
+// The method (FlashAttention milestone page (nlp-lineage), "The idea -- Tiling";
+// FlashAttention proof-of-work page, "SRAM Block Tiling" and "Online Softmax
+// Computation"): split Q, K and V into blocks that fit on chip, stream K/V
+// blocks past a resident Q block, keep a running row max m and row sum l, and
+// rescale the earlier partial output when m grows, so that the result equals
+// standard attention exactly. Only O and one log-sum-exp per row leave the
+// chip (milestone page, "The idea -- Recomputation").
+//
+// GB300 design (not the pages' A100 design):
+//   * one CTA owns two 128-row Q tiles of one (batch, head); 10 warps:
+//       warps 0-3  softmax / correction / epilogue of Q tile 0 (TMEM lanes 0-127)
+//       warps 4-7  the same for Q tile 1
+//       warp  8    TMA producer (Q once, then a K ring and a V ring)
+//       warp  9    TMEM allocator and the single thread that issues tcgen05.mma
+//   * S_t = Q_t K_j^T accumulates in TMEM (128 fp32 columns per Q tile); the
+//     softmax warps overwrite it in place with P_t as packed bf16, which the
+//     tensor core then reads straight from TMEM for O_t += P_t V_j;
+//   * O_t accumulates in TMEM for the whole K/V sweep and is written once;
+//   * the two Q tiles ping-pong: while one softmax group works on its S, the
+//     tensor core runs the other tile's P V and next S;
+//   * the MMA thread is event driven: each Q tile walks only its own live key
+//     tiles (causal, key-length and block-sparse skipping are exact per tile),
+//     while K/V tiles are loaded once for the pair.
+//   * the running max is moved (and O rescaled) only when a new row max
+//     exceeds it by more than 2^8; the final O / l and LSE use the same
+//     reference max, so the result is unchanged.
+#include "fa_common.cuh"
+#include "fa_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace fa {
+
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr int kListMax = kMaxN / kTile;   // union list capacity
+constexpr float kRescaleThreshold = 8.0f; // log2 units
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kHalves = D / 64;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBar = kV + kStages * kTileBytes;   // 8-byte mbarriers
+  // barrier slots
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + kStages;
+  static constexpr int bVFull = bKEmpty + kStages;
+  static constexpr int bVEmpty = bVFull + kStages;
+  static constexpr int bSFull = bVEmpty + kStages;    // [2]
+  static constexpr int bPFull = bSFull + 2;           // [2]
+  static constexpr int bOFinal = bPFull + 2;          // [2]
+  static constexpr int bDrain = bOFinal + 2;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort, list length
+  static constexpr int kList = kMisc + 16;
+  static constexpr int kEnd = kList + 4 * kListMax;
+  static constexpr int kSmemBytes = kEnd + 1024;      // + alignment slack
+};
+
+__device__ __forceinline__ int entry_j(uint32_t e) { return (int)(e & 0xFFFFu); }
+__device__ __forceinline__ uint32_t entry_live(uint32_t e, int t) { return (e >> (16 + t)) & 1u; }
+__device__ __forceinline__ uint32_t entry_partial(uint32_t e, int t) { return (e >> (18 + t)) & 1u; }
+__device__ __forceinline__ uint32_t entry_nlive(uint32_t e) {
+  return entry_live(e, 0) + entry_live(e, 1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+              const FwdParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int BH = p.B * p.H;
+  const int nC = (p.nT + 1) >> 1;
+  const int L_ = blockIdx.x;
+  const int c = nC - 1 - L_ / BH;        // heaviest Q-tile pairs first
+  const int bh = L_ % BH;
+  const int b = bh / p.H;
+  const int kvl = effective_kv_len(p.kv_len, b, p.N);
+  const int qi0 = 2 * c;
+  const bool has_t1 = (qi0 + 1) < p.nT;
+
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  uint32_t* list = reinterpret_cast<uint32_t*>(smem + L::kList);
+  Ctl ctl{p.err, abort_flag};
+
+  if (tid == 0) {
+    for (int i = 0; i < L::kNumBars; ++i)
+      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 128u : 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(misc), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8) {
+    // union list of live key tiles of the two Q tiles, ascending j
+    int count = 0;
+    for (int base = 0; base < p.nT; base += 32) {
+      const int j = base + lane;
+      uint32_t e = 0;
+      if (j < p.nT) {
+        const int s0 = tile_state(qi0, j, kvl, p.nT, p.causal, p.block_mask);
+        const int s1 = has_t1 ? tile_state(qi0 + 1, j, kvl, p.nT, p.causal, p.block_mask) : kSkip;
+        e = (uint32_t)j | ((s0 != kSkip) ? (1u << 16) : 0u) | ((s1 != kSkip) ? (1u << 17) : 0u) |
+            ((s0 == kPartial) ? (1u << 18) : 0u) | ((s1 == kPartial) ? (1u << 19) : 0u);
+      }
+      const bool live = (e >> 16) & 3u;
+      const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
+      if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = e;
+      count += __popc(ball);
+    }
+    if (lane == 0) misc[2] = (uint32_t)count;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = misc[0];
+  const int len = (int)misc[2];
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tq);
+      tma_prefetch_map(&tk);
+      tma_prefetch_map(&tv);
+      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
+      mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
+      for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
+                      kTile * (qi0 + t), bh);
+      int nk = 0, nv = 0;   // K and V loads issued
+      for (int e = 0; e < len; ++e) {
+        const int s = e % L::kStages;
+        const uint32_t n = (uint32_t)(e / L::kStages);
+        const int j = entry_j(list[e]);
+        if (e >= L::kStages && !mbar_wait(bar(L::bKEmpty + s), (n - 1) & 1u, ctl, 1)) break;
+        mbar_arrive_expect_tx(bar(L::bKFull + s), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kK + s * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + s),
+                      64 * h, kTile * j, bh);
+        ++nk;
+        if (e >= L::kStages && !mbar_wait(bar(L::bVEmpty + s), (n - 1) & 1u, ctl, 2)) break;
+        mbar_arrive_expect_tx(bar(L::bVFull + s), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kV + s * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + s),
+                      64 * h, kTile * j, bh);
+        ++nv;
+      }
+      // every load issued must have landed before the CTA may exit
+      drain_wait(bar(L::bQFull), 0);
+      for (int s = 0; s < L::kStages; ++s) {
+        if (s < nk) drain_wait(bar(L::bKFull + s), (uint32_t)((s + ((nk - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+        if (s < nv) drain_wait(bar(L::bVFull + s), (uint32_t)((s + ((nv - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+      const uint32_t sQ[2] = {sbase + L::kQ, sbase + L::kQ + L::kTileBytes};
+      int pos[2], st[2], npv[2];
+      uint32_t kdone[L::kStages], vdone[L::kStages];
+      for (int s = 0; s < L::kStages; ++s) { kdone[s] = 0; vdone[s] = 0; }
+      enum { kNeedS = 0, kNeedP = 1, kDone = 2 };
+      for (int t = 0; t < 2; ++t) {
+        int e = 0;
+        while (e < len && !entry_live(list[e], t)) ++e;
+        pos[t] = e;
+        st[t] = (e < len) ? kNeedS : kDone;
+        npv[t] = 0;
+      }
+      bool ok = mbar_wait(bar(L::bQFull), 0, ctl, 4);
+      tc_fence_after();
+      uint64_t idle_t0 = globaltimer();
+      uint32_t idle = 0;
+      while (ok && (st[0] != kDone || st[1] != kDone)) {
+        bool progressed = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (st[t] == kNeedS) {
+            const int e = pos[t];
+            const int s = e % L::kStages;
+            const uint32_t ph = (uint32_t)(e / L::kStages) & 1u;
+            if (mbar_test(bar(L::bKFull + s), ph)) {
+              tc_fence_after();
+              const uint32_t sK = sbase + L::kK + s * L::kTileBytes;
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_ss(tS[t], desc_kmajor(sQ[t], ks), desc_kmajor(sK, ks), idS, ks > 0 ? 1u : 0u);
+              mma_commit(bar(L::bSFull + t));
+              if (++kdone[s] == entry_nlive(list[e])) {
+                kdone[s] = 0;
+                mma_commit(bar(L::bKEmpty + s));
+              }
+              st[t] = kNeedP;
+              progressed = true;
+            }
+          } else if (st[t] == kNeedP) {
+            const int e = pos[t];
+            const int s = e % L::kStages;
+            const uint32_t ph = (uint32_t)(e / L::kStages) & 1u;
+            if (mbar_test(bar(L::bPFull + t), (uint32_t)npv[t] & 1u) &&
+                mbar_test(bar(L::bVFull + s), ph)) {
+              tc_fence_after();
+              const uint32_t sV = sbase + L::kV + s * L::kTileBytes;
+#pragma unroll
+              for (int ks = 0; ks < kTile / 16; ++ks)
+                mma_ts(tO[t], tS[t] + (uint32_t)ks * 8u, desc_mnmajor(sV, ks), idO,
+                       (npv[t] > 0 || ks > 0) ? 1u : 0u);
+              ++npv[t];
+              if (++vdone[s] == entry_nlive(list[e])) {
+                vdone[s] = 0;
+                mma_commit(bar(L::bVEmpty + s));
+              }
+              int n = e + 1;
+              while (n < len && !entry_live(list[n], t)) ++n;
+              pos[t] = n;
+              if (n < len) {
+                st[t] = kNeedS;
+              } else {
+                mma_commit(bar(L::bOFinal + t));
+                st[t] = kDone;
+              }
+              progressed = true;
+            }
+          }
+        }
+        if (progressed) {
+          idle = 0;
+          idle_t0 = globaltimer();
+        } else if ((++idle & 63u) == 0u) {
+          if (*abort_flag) break;
+          if (globaltimer() - idle_t0 > kWaitLimitNs) {
+            report_error(ctl, kErrTimeout, 5);
+            break;
+          }
+        }
+      }
+      // every MMA this thread issued must be complete before TMEM is freed
+      mma_commit(bar(L::bDrain));
+      drain_wait(bar(L::bDrain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax groups
+    const int t = warp >> 2;                 // Q tile of this warpgroup
+    const int r = tid & 127;                 // row within the tile = TMEM lane
+    const int qi = qi0 + t;
+    const int row = kTile * qi + r;          // query index within the head
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_off;
+    const uint32_t tO = tmem + 256u + (uint32_t)(t * D) + lane_off;
+    const float sl2 = p.scale_log2;
+
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    uint32_t n = 0;
+    bool ok = (qi < p.nT);
+    for (int e = 0; e < len && ok; ++e) {
+      const uint32_t ent = list[e];
+      if (!entry_live(ent, t)) continue;
+      if (!mbar_wait_warp(bar(L::bSFull + t), n & 1u, ctl, 10 + t)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(tS + 0u, u0);
+        tmem_ld32(tS + 32u, u1);
+        tmem_ld32(tS + 64u, u2);
+        tmem_ld32(tS + 96u, u3);
+        tmem_ld_wait(u0);
+        tmem_ld_wait(u1);
+        tmem_ld_wait(u2);
+        tmem_ld_wait(u3);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(u0[i]);
+          x[32 + i] = __uint_as_float(u1[i]);
+          x[64 + i] = __uint_as_float(u2[i]);
+          x[96 + i] = __uint_as_float(u3[i]);
+        }
+      }
+      if (entry_partial(ent, t)) {
+        const int key0 = kTile * entry_j(ent);
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int key = key0 + i;
+          if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
+        }
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+      const float m_new = mx * sl2;
+      // move the reference max only when the row max grew by more than the
+      // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
+      // warp rescales when any of its rows needs it (alpha = 1 for the rest)
+      const bool move = (n == 0) || (m_new > m_ref + kRescaleThreshold);
+      float alpha = 1.f;
+      if (move) {
+        alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
+        uint32_t u[32];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          tmem_ld32(tO + 32u * cc, u);
+          tmem_ld_wait(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + 32u * cc, u);
+        }
+        tmem_st_wait();
+      }
+      const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sum = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(x[64 * hh + 2 * i], sl2, -ref));
+          const float p1 = ex2(fmaf(x[64 * hh + 2 * i + 1], sl2, -ref));
+          sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32u * hh, pk);
+      }
+      tmem_st_wait();
+      l += sum;
+      tc_fence_before();
+      mbar_arrive(bar(L::bPFull + t));
+      ++n;
+    }
+
+    if (qi < p.nT) {
+      // all MMAs that read Q_t have completed (or never ran); make sure the
+      // Q load itself has landed before its buffer is reused for staging O
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (ok) ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 12 + t);
+      if (ok && n > 0) ok = mbar_wait_warp(bar(L::bOFinal + t), 0, ctl, 14 + t);
+      tc_fence_after();
+      uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
+      const float inv_l = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
+      const bool have_o = ok && n > 0;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (have_o) {
+          tmem_ld32(tO + 32u * cc, u);
+          tmem_ld_wait(u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
+        // 32 columns = 4 chunks of 16 bytes, 128B-swizzled rows
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = 32 * cc + 8 * k;           // first column of the chunk
+          const int h = col >> 6;                    // 64-column half
+          const int chunk = (col & 63) >> 3;         // chunk within the 128-byte row
+          uint8_t* dst = stage + h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      if (row < p.N) {
+        float lse = -INFINITY;
+        if (have_o && l > 0.f) lse = (m_ref + log2f(l)) * 0.69314718055994531f;
+        p.lse[(size_t)bh * p.N + row] = lse;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (r == 0) {
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_store_3d(&to, smem_u32(stage) + h * 16384, 64 * h, kTile * qi, bh);
+        bulk_commit_group();
+        bulk_wait_group_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
+  using L = FwdLayout<D>;
+  static bool configured = false;   // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int nC = (p.nT + 1) / 2;
+  const dim3 grid((unsigned)(nC * p.B * p.H));
+  fa_fwd_kernel<D><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, p, s);
+  return launch_fwd_d<128>(tq, tk, tv, to, p, s);
+}
+
+}  // namespace fa

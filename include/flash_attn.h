@@ -1,0 +1,133 @@
+/*
+ * flash_attn.h -- C ABI of an exact, IO-aware attention library for NVIDIA
+ * GB300 (sm_103a): forward and backward of
+ *
+ *     O = softmax(scale * Q K^T + mask) V
+ *
+ * computed tile by tile with an online softmax, never storing the N x N score
+ * matrix (FlashAttention milestone page (nlp-lineage), "The notation" and
+ * "The idea"; FlashAttention proof-of-work page, "SRAM Block Tiling",
+ * "Online Softmax Computation", "Activation Gradient Recomputation").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are row-major, contiguous, one (batch, head) after another:
+ *      Q, K, V, O, dO, dQ, dK, dV : bfloat16 [B, H, N, d]
+ *      LSE                         : float32  [B, H, N]
+ *    N is the sequence length of both queries and keys. d is 64 or 128.
+ *  - Every pointer named here is a DEVICE pointer of the current CUDA device,
+ *    16-byte aligned, owned by the caller (the library keeps no reference
+ *    after the call returns and allocates no device memory).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream). Argument errors are returned before anything is
+ *    launched; launch errors are returned as FA_ERR_CUDA. Errors that arise
+ *    on the device (a bounded wait that ran out) are recorded in a device
+ *    error word read by flash_attn_get_device_error() after the stream has
+ *    been synchronised.
+ *  - Masks combine by AND. Key j takes part in query row i's softmax when
+ *      (causal == 0 || j <= i)  and  j < kv_len[b]  and
+ *      block_mask[(i / 128) * nT + (j / 128)] != 0,       nT = ceil(N / 128).
+ *    kv_len (device int32 [B], values clamped to [0, N]) and block_mask
+ *    (device uint8 [nT, nT], shared by all batches and heads; the block-sparse
+ *    pattern whose empty blocks are skipped -- milestone page, "The idea")
+ *    may each be NULL, meaning "no such mask". Tiles with no allowed pair
+ *    are skipped entirely.
+ *  - A query row with no allowed key gets O = 0, LSE = -inf and dQ = 0.
+ *  - Every output element is written; outputs need no initialisation.
+ */
+#ifndef FLASH_ATTN_H
+#define FLASH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size, non-finite scale */
+  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 128}, N > 131072, no sm_103a device */
+  FA_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small */
+  FA_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 5,   /* a kernel's bounded wait ran out (device error word) */
+  FA_ERR_DEVICE_INTERNAL = 6   /* a kernel found its shared memory misaligned */
+} fa_status;
+
+/*
+ * Forward pass. Computes, for every (b, h) and query row i,
+ *   O[b,h,i,:]  = sum_j P_ij V[b,h,j,:],  P_ij = exp(S_ij - LSE[b,h,i]),
+ *   LSE[b,h,i]  = ln sum_j exp(S_ij),     S_ij = scale * Q[b,h,i,:] . K[b,h,j,:]
+ * over the allowed keys j (natural logarithm, scaled scores). Only O and LSE
+ * are written (milestone page, "The idea -- Recomputation": the output and the
+ * softmax statistics are all the backward pass needs).
+ *   Q, K, V : in,  bf16 [B, H, N, d]
+ *   O       : out, bf16 [B, H, N, d]
+ *   LSE     : out, fp32 [B, H, N]
+ *   B, H >= 1; 1 <= N <= 131072; d in {64, 128}; scale finite;
+ *   causal 0 or 1; kv_len, block_mask as above (may be NULL).
+ */
+fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t* kv_len, const uint8_t* block_mask, void* stream);
+
+/*
+ * Bytes of device workspace flash_attn_bwd needs for this shape (fp32 dQ
+ * accumulator [B, H, nT*128, d] plus two fp32 row vectors [B, H, nT*128]).
+ * Returns 0 for an invalid shape.
+ */
+size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass by recomputation: given the forward's inputs, its outputs O
+ * and LSE, and the output gradient dO, writes
+ *   dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q,
+ *   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+ * recomputing S and P block by block on chip (milestone page, "The idea --
+ * Recomputation"; the gradient formulas are the textbook derivative of
+ * L = sum(dO * O), which the pages do not spell out).
+ *   Q, K, V, O, dO : in,  bf16 [B, H, N, d];  LSE : in, fp32 [B, H, N]
+ *   dQ, dK, dV     : out, bf16 [B, H, N, d]
+ *   workspace      : device scratch of at least
+ *                    flash_attn_bwd_workspace_size(B, H, N, d) bytes,
+ *                    256-byte aligned, owned by the caller; its contents on
+ *                    entry do not matter and on exit are unspecified.
+ *   Other arguments as in flash_attn_fwd; they must match the forward call
+ *   that produced O and LSE.
+ */
+fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t* kv_len, const uint8_t* block_mask,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The tile classifier the kernels use to decide which 128 x 128 tiles to
+ * compute: writes out[b, qi, kj] (device uint8 [B, nT, nT]) as
+ *   0 = skipped (no allowed pair), 1 = full (every pair allowed),
+ *   2 = partial (computed with element masking).
+ * Rows past N do not count; keys past N count as masked.
+ */
+fa_status flash_attn_tile_map(int B, int N, int causal, const int32_t* kv_len,
+                              const uint8_t* block_mask, uint8_t* out, void* stream);
+
+/*
+ * Reads and clears the device error word of the current device. Call after
+ * synchronising the streams used. Returns FA_OK when no kernel reported an
+ * error. If detail is not NULL it receives 4 host uint32 values:
+ * {code, site, block, thread} of the first error recorded.
+ */
+fa_status flash_attn_get_device_error(uint32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* flash_attn_status_string(fa_status status);
+
+/* Library ABI version: 100 * major + minor. */
+int flash_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASH_ATTN_H */

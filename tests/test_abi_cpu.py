@@ -1,0 +1,81 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and its host-only calls (version, status strings, workspace
+sizing, argument validation) behave as documented. No kernel is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_39_gb300 import build as b
+    path = b.build()
+    import exact_io_aware_39_gb300._lib as L
+    return L.load(path)
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "flash_attn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(flash_attn_\w+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    names = _declared()
+    assert names and set(names) == set(L.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", out, flags=re.M), n
+
+
+def test_version_and_status_strings(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    assert L.flash_attn_version() == 100
+    assert L.flash_attn_status_string(0) == "ok"
+    assert "workspace" in L.flash_attn_status_string(3)
+    assert L.flash_attn_status_string(99) == "unknown status"
+
+
+def test_workspace_size_formula(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    def al(x):
+        return (x + 255) // 256 * 256
+    for B, H, N, d in [(1, 2, 256, 64), (2, 3, 300, 128), (1, 32, 16384, 128)]:
+        Np = (N + 127) // 128 * 128
+        want = al(al(B * H * Np * d * 4) + B * H * Np * 4) + al(B * H * Np * 4)
+        assert L.flash_attn_bwd_workspace_size(B, H, N, d) == want
+    assert L.flash_attn_bwd_workspace_size(1, 1, 256, 96) == 0
+    assert L.flash_attn_bwd_workspace_size(0, 1, 256, 64) == 0
+
+
+@pytest.mark.parametrize("B,H,N,d,scale,causal,want", [
+    (0, 1, 128, 64, 0.1, 0, 1), (1, 0, 128, 64, 0.1, 0, 1), (1, 1, 0, 64, 0.1, 0, 1),
+    (1, 1, 128, 64, float("nan"), 0, 1), (1, 1, 128, 64, float("inf"), 0, 1),
+    (1, 1, 128, 64, 0.1, 2, 1), (1, 1, 128, 96, 0.1, 0, 2), (1, 1, 131073, 64, 0.1, 0, 2),
+])
+def test_invalid_shapes_rejected_before_any_launch(lib, B, H, N, d, scale, causal, want):
+    from exact_io_aware_39_gb300 import _lib as L
+    p = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    st = L.flash_attn_fwd(p, p, p, p, p, B, H, N, d, scale, causal, None, None, None)
+    assert st == want
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    p = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    assert L.flash_attn_fwd(None, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, None) == 1
+    assert L.flash_attn_fwd(p, p, bad, p, p, 1, 1, 128, 64, 0.1, 0, None, None, None) == 1
+    ws = L.flash_attn_bwd_workspace_size(1, 1, 128, 64)
+    args = [p] * 9 + [1, 1, 128, 64, 0.1, 0, None, None]
+    assert L.flash_attn_bwd(*args, p, ws - 1, None) == 3          # too small
+    assert L.flash_attn_bwd(*args, bad, ws, None) == 3            # misaligned
+    assert L.flash_attn_bwd(*args, None, ws, None) == 3           # missing
