@@ -1,0 +1,419 @@
+"""Throughput of exact attention, forward + backward, on GB300.
+
+One step = one pass of the whole hot path (forward kernel, then the three
+backward kernels) over one batch of the workload's synthetic inputs. Prints
+ONE JSON line on stdout (rank 0):
+
+  value        whole-job TFLOP/s (algorithmic FLOP over allowed pairs: 4 d per
+               pair forward, 10 d backward), inputs resident in HBM, timed with
+               CUDA events around each step on the launching stream
+  e2e          the same metric through the public API with pinned host
+               buffers: host-to-device copies of Q, K, V, dO and device-to-host
+               copies of O, LSE, dQ, dK, dV inside every timed step
+  roofline     the backward main kernel (the dominant launch) against the
+               measured dense bf16 tensor peak
+  cpu_baseline the CPU float64 oracle on a bounded sample of the same workload
+
+`--impl reference` times the oracle itself (the CPU reference arm) on the
+same workload and metric. Several GPUs (torchrun) run independent replicas:
+the heads of different ranks never interact, so there is no collective on the
+data path, only a barrier and a max-reduction of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_causal")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N override of the workload (smaller cases for profiler captures)")
+    return ap.parse_args()
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _workload_config(w, extra=None):
+    cfg = {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} d={w.d} "
+                       f"{'causal' if w.causal else 'non-causal'}"
+                       + (f", kv_len~U{{{w.kv_len_range[0]}..{w.kv_len_range[1]}}}" if w.kv_len_range else "")
+                       + (f", 128x128 block mask p={w.block_p} diagonal on" if w.block_p else ""),
+           "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "scale": w.scale}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+def _traffic_record(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for rel in rec["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec["sha256"]:
+        return None
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples around the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark(self, start):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        # samples under load: the timed region is GPU-saturated; take the samples
+        # with the GPU busy (power well above idle)
+        pmax = max(r["power"] for r in rows)
+        loaded = [r for r in rows if r["power"] >= 0.5 * pmax] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in loaded),
+                "reasons": sorted(reasons), "samples": len(loaded),
+                "power_w_max": max(r["power"] for r in loaded)}
+
+
+def _oracle_once(w, c, n_rows):
+    import oracle
+    from exact_io_aware_39_gb300.flops import allowed_pairs
+    sl = slice(0, n_rows)
+    q, k, v, do = (c[n][:, :, sl] for n in ("q", "k", "v", "do"))
+    nT = (n_rows + 127) // 128
+    bm = None if c["block_mask"] is None else c["block_mask"][:nT, :nT]
+    kv = None if c["kv_len"] is None else c["kv_len"].clamp(max=n_rows)
+    t0 = time.perf_counter()
+    oracle.attention_fwd_bwd(q, k, v, do, w.scale, w.causal, kv, bm, heads=[(0, 0)])
+    dt = time.perf_counter() - t0
+    pairs = int(allowed_pairs(1, n_rows, w.causal, None if kv is None else kv[:1].numpy(),
+                              None if bm is None else bm.numpy())[0])
+    return dt, 14 * w.d * pairs     # fwd 4 d + bwd 10 d FLOP per allowed pair
+
+
+def _cpu_oracle_sample(w, budget_s):
+    """Times the CPU float64 oracle (fwd + bwd, S and P materialised) on a
+    bounded sample of the workload: one head (b = 0, h = 0); for a causal
+    workload whose full head would exceed the time budget, the first n rows
+    of that head, which under the causal mask are an exact sub-problem (they
+    see only keys < n). Returns (TFLOP/s, description, cores, seconds)."""
+    from exact_io_aware_39_gb300.inputs import make_case
+    c = make_case(w, B=1 if w.kv_len_range is None else w.B, H=1)
+    cores = len(os.sched_getaffinity(0))
+    n_rows = w.N
+    if w.causal and w.N >= 2048:
+        probe = max(256, (w.N // 8) // 128 * 128)
+        t8, _ = _oracle_once(w, c, probe)
+        est = t8 * (w.N / probe) ** 2
+        if est > budget_s:
+            n_rows = int(probe * math.sqrt(budget_s / max(t8, 1e-6))) // 128 * 128
+            n_rows = max(probe, min(w.N, n_rows))
+    dt, flop = _oracle_once(w, c, n_rows)
+    desc = (f"head (b=0, h=0), fwd+bwd" + ("" if n_rows == w.N else f", first {n_rows} of {w.N} rows (causal prefix)")
+            + f", {dt:.2f} s, numpy float64")
+    return flop / dt / 1e12, desc, cores, dt
+
+
+def run_reference(args):
+    """CPU reference arm: the float64 oracle, as it stands, on the host cores."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return
+    from exact_io_aware_39_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    times, rates = [], []
+    desc, cores = "", 1
+    budget = max(0.5, 150.0 / max(1, args.steps + min(args.warmup, 1)))
+    for i in range(min(args.warmup, 1) + args.steps):   # one untimed warm-up sample is enough on a CPU
+        r, desc, cores, dt = _cpu_oracle_sample(w, budget)
+        if i >= min(args.warmup, 1):
+            times.append(dt)
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic N(0,1), seeded", "config": _workload_config(w, {"sample": desc}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import exact_io_aware_39_gb300 as fa
+    from exact_io_aware_39_gb300 import build as _build
+    from exact_io_aware_39_gb300.flops import attention_flops
+    from exact_io_aware_39_gb300.inputs import WORKLOADS, make_case
+    fa.load(_build.build() if rank == 0 or world == 1 else _build.LIB_PATH)
+
+    w = WORKLOADS[args.workload]
+    if args.shape:
+        import dataclasses
+        sb, sh, sn = (int(x) for x in args.shape.split(","))
+        w = dataclasses.replace(w, B=sb, H=sh, N=sn, name=f"{w.name}@{sb}x{sh}x{sn}")
+    c = make_case(w)
+    B, H, N, d = c["B"], c["H"], c["N"], c["d"]
+    kv_np = None if c["kv_len"] is None else c["kv_len"].numpy()
+    bm_np = None if c["block_mask"] is None else c["block_mask"].numpy()
+    f_fwd, f_bwd = attention_flops(B, H, N, d, w.causal, kv_np, bm_np)
+    flop_step = f_fwd + f_bwd
+
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    kv = None if c["kv_len"] is None else c["kv_len"].to(dev)
+    bm = None if c["block_mask"] is None else c["block_mask"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.flash_attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    in_bytes = 4 * q.numel() * 2
+    flush = in_bytes < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse)
+        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, detail = fa.device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {detail}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in ev:          # create the underlying CUDA events
+        for e in row:
+            e.record(stream)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    barrier()
+    if sampler:
+        sampler.mark(True)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        if flush:
+            scratch.zero_()     # evict the inputs from L2 between steps (outside the events)
+        e = ev[i]
+        e[0].record(stream)
+        fa.profile_next_call(e[1], e[2])
+        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse)
+        fa.profile_next_call(e[3], e[4])
+        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv)
+        e[5].record(stream)
+    barrier()
+    wall1 = time.perf_counter()
+    if sampler:
+        sampler.mark(False)
+    step_ms = [ev[i][0].elapsed_time(ev[i][5]) for i in range(K)]
+    fwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    bwd_main_ms = [ev[i][3].elapsed_time(ev[i][4]) for i in range(K)]
+    total_ms = sum(step_ms)
+    st, detail = fa.device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during timing: {detail}")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * flop_step * K / (total_ms * 1e-3) / 1e12
+    clocks = sampler.stop() if sampler else None
+
+    # end-to-end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+        gq, gk, gv, gdo = (torch.empty_like(q) for _ in range(4))
+
+        def e2e_step():
+            for g, h in ((gq, hq), (gk, hk), (gv, hv), (gdo, hdo)):
+                g.copy_(h, non_blocking=True)
+            fa.attention_fwd(gq, gk, gv, w.scale, w.causal, kv, bm, out=o, lse=lse)
+            fa.attention_bwd(gq, gk, gv, o, gdo, lse, w.scale, w.causal, kv, bm, workspace=ws,
+                             dq=dq, dk=dk, dv=dv)
+            for h, g in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                h.copy_(g, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        Ke = max(3, K // 2)
+        ea.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        eb.record(stream)
+        barrier()
+        e2e_ms = ea.elapsed_time(eb)
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flop_step * Ke / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / Ke}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak_burst, peak_sust, peak_src = _peaks()
+    timed_s = total_ms * 1e-3
+    peak = peak_sust if timed_s > 2.0 else peak_burst
+    bwd_avg = statistics.mean(bwd_main_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    achieved = f_bwd / (bwd_avg * 1e-3) / 1e12
+    tr = _traffic_record(f"bwd_main:{w.name}")
+    roofline = {"kernel": "fa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{'sustained' if peak == peak_sust else 'burst'} bf16, {peak_src}",
+                "traffic": None if tr is None else tr["dram_bytes_per_launch"],
+                "fwd_kernel": {"achieved": f_fwd / (fwd_avg * 1e-3) / 1e12,
+                               "frac": f_fwd / (fwd_avg * 1e-3) / 1e12 / peak, "ms": fwd_avg},
+                "bwd_main_ms": bwd_avg}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, desc, cores, _ = _cpu_oracle_sample(w, 15.0)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic N(0,1) bf16, seeded (no dataset)",
+            "config": _workload_config(w, {
+                "l2": "L2 flushed between steps" if flush else "inputs larger than L2 (not flushed)",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+                "flop_per_step": flop_step, "fwd_flop": f_fwd, "bwd_flop": f_bwd}),
+            "pct_of_peak": 100.0 * value / world / peak,
+            "gpu_launches": 4 * K,
+            "timed_wall_s": wall1 - wall0,
+            "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

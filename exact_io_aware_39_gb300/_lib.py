@@ -22,7 +22,8 @@ STATUS_NAMES = {
 # every symbol include/flash_attn.h declares
 EXPORTS = [
     "flash_attn_fwd", "flash_attn_bwd_workspace_size", "flash_attn_bwd", "flash_attn_tile_map",
-    "flash_attn_get_device_error", "flash_attn_status_string", "flash_attn_version",
+    "flash_attn_get_device_error", "flash_attn_set_profile_events", "flash_attn_status_string",
+    "flash_attn_version",
 ]
 
 
@@ -54,6 +55,8 @@ def load(path=LIB_PATH):
     lib.flash_attn_tile_map.restype = i32
     lib.flash_attn_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.flash_attn_get_device_error.restype = i32
+    lib.flash_attn_set_profile_events.argtypes = [vp, vp]
+    lib.flash_attn_set_profile_events.restype = i32
     lib.flash_attn_status_string.argtypes = [i32]
     lib.flash_attn_status_string.restype = ctypes.c_char_p
     lib.flash_attn_version.argtypes = []
@@ -88,6 +91,10 @@ def flash_attn_get_device_error():
     detail = (ctypes.c_uint32 * 4)()
     st = load().flash_attn_get_device_error(detail)
     return st, list(detail)
+
+
+def flash_attn_set_profile_events(start_event, stop_event):
+    return load().flash_attn_set_profile_events(start_event, stop_event)
 
 
 def flash_attn_status_string(status):
@@ -183,6 +190,13 @@ def tile_map(B, N, causal=False, kv_len=None, block_mask=None, device="cuda", st
     st = flash_attn_tile_map(B, N, int(bool(causal)), kv_p, bm_p, _ptr(out), _stream(stream))
     _check(st, "flash_attn_tile_map")
     return out
+
+
+def profile_next_call(start, stop):
+    """Record torch.cuda.Event start/stop around the dominant kernel of the
+    next attention_fwd/attention_bwd call of this thread."""
+    st = flash_attn_set_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
+    _check(st, "flash_attn_set_profile_events")
 
 
 def device_error():

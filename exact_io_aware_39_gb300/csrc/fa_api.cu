@@ -28,6 +28,20 @@ struct DeviceState {
   unsigned int* err = nullptr;
 };
 
+// events recorded around the dominant kernel of the next call of this thread
+thread_local cudaEvent_t t_prof_start = nullptr;
+thread_local cudaEvent_t t_prof_stop = nullptr;
+
+struct ProfileScope {
+  cudaEvent_t a, b;
+  cudaStream_t s;
+  explicit ProfileScope(cudaStream_t st) : a(t_prof_start), b(t_prof_stop), s(st) {
+    t_prof_start = t_prof_stop = nullptr;
+  }
+  void before() const { if (a) cudaEventRecord(a, s); }
+  void after() const { if (b) cudaEventRecord(b, s); }
+};
+
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
@@ -146,8 +160,11 @@ fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, f
   p.nT = (N + kTile - 1) / kTile;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
-                                                                                             : FA_ERR_CUDA;
+  const ProfileScope prof(static_cast<cudaStream_t>(stream));
+  prof.before();
+  const cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  prof.after();
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d) {
@@ -194,7 +211,11 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
   p.nT = nT;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  if (launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s) != cudaSuccess) return FA_ERR_CUDA;
+  const ProfileScope prof(s);
+  prof.before();
+  const cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s);
+  prof.after();
+  if (e != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_dq(dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -224,6 +245,13 @@ fa_status flash_attn_get_device_error(uint32_t* detail) {
   if (h[0] == 0) return FA_OK;
   if (h[0] == kErrTimeout) return FA_ERR_DEVICE_TIMEOUT;
   return FA_ERR_DEVICE_INTERNAL;
+}
+
+fa_status flash_attn_set_profile_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return FA_ERR_INVALID_ARG;
+  t_prof_start = static_cast<cudaEvent_t>(start_event);
+  t_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return FA_OK;
 }
 
 const char* flash_attn_status_string(fa_status s) {

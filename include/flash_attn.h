@@ -120,6 +120,18 @@ fa_status flash_attn_tile_map(int B, int N, int causal, const int32_t* kv_len,
  */
 fa_status flash_attn_get_device_error(uint32_t* detail);
 
+/*
+ * Profiling hook (no counterpart on the pages; for timing the kernels with
+ * CUDA events on the stream they run on). start_event and stop_event are
+ * cudaEvent_t handles created by the caller. Once set, the next
+ * flash_attn_fwd or flash_attn_bwd call made by this host thread records
+ * start_event on its stream immediately before its dominant kernel (the
+ * forward kernel, or the backward main kernel) and stop_event immediately
+ * after it, then forgets both. Passing NULL, NULL clears a pending setting.
+ * Returns FA_ERR_INVALID_ARG if exactly one handle is NULL.
+ */
+fa_status flash_attn_set_profile_events(void* start_event, void* stop_event);
+
 /* Human-readable name of a status code (static storage). */
 const char* flash_attn_status_string(fa_status status);
 
