@@ -17,11 +17,15 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
     4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT", 6: "FA_ERR_DEVICE_INTERNAL",
+    7: "FA_ERR_SCRATCH_LIMIT",
 }
+FA_ERR_SCRATCH_LIMIT = 7
+BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # every symbol include/flash_attn.h declares
 EXPORTS = [
-    "flash_attn_fwd", "flash_attn_bwd_workspace_size", "flash_attn_bwd", "flash_attn_tile_map",
+    "flash_attn_fwd", "flash_attn_bwd_workspace_size", "flash_attn_bwd", "flash_attn_bwd_noalloc",
+    "flash_attn_tile_map",
     "flash_attn_get_device_error", "flash_attn_set_profile_events", "flash_attn_status_string",
     "flash_attn_version",
 ]
@@ -51,6 +55,8 @@ def load(path=LIB_PATH):
     lib.flash_attn_bwd_workspace_size.restype = sz
     lib.flash_attn_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]
     lib.flash_attn_bwd.restype = i32
+    lib.flash_attn_bwd_noalloc.argtypes = [vp] * 9 + [i32, i32, i32, i32, f32, i32, vp, vp, vp]
+    lib.flash_attn_bwd_noalloc.restype = i32
     lib.flash_attn_tile_map.argtypes = [i32, i32, i32, vp, vp, vp, vp]
     lib.flash_attn_tile_map.restype = i32
     lib.flash_attn_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -81,6 +87,14 @@ def flash_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, k
                    workspace, workspace_bytes, stream):
     return load().flash_attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len,
                                  block_mask, workspace, workspace_bytes, stream)
+
+
+def flash_attn_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len,
+                           block_mask, stream):
+    """Backward without a workspace argument: for callers that cannot allocate
+    device memory (see the header); scratch comes from a fixed 64 MiB array."""
+    return load().flash_attn_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
+                                         kv_len, block_mask, stream)
 
 
 def flash_attn_tile_map(B, N, causal, kv_len, block_mask, out, stream):

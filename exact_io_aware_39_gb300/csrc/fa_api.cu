@@ -120,6 +120,22 @@ __global__ void tile_map_kernel(int B, int N, int nT, int causal, const int32_t*
 
 }  // namespace
 
+// Internal accessors for other translation units of the library.
+int internal_check_shape(int B, int H, int N, int d, float scale, int causal) {
+  return check_shape(B, H, N, d, scale, causal);
+}
+
+int internal_device_error_word(unsigned int** err) {
+  DeviceState* ds = nullptr;
+  const fa_status st = device_state(&ds);
+  if (st == FA_OK) *err = ds->err;
+  return st;
+}
+
+int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  return make_map(m, base, BH, N, d);
+}
+
 cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len, const uint8_t* block_mask,
                             uint8_t* out, cudaStream_t s) {
   const long long total = (long long)B * nT * nT;
@@ -263,6 +279,7 @@ const char* flash_attn_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case FA_ERR_DEVICE_INTERNAL: return "device internal error";
+    case FA_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the fixed no-alloc scratch array";
   }
   return "unknown status";
 }

@@ -82,6 +82,11 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, in
 cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len,
                             const uint8_t* block_mask, uint8_t* out, cudaStream_t s);
 
+// Host helpers defined with the C ABI (return fa_status values).
+int internal_check_shape(int B, int H, int N, int d, float scale, int causal);
+int internal_device_error_word(unsigned int** err);   // current device; runs its set-up once
+int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d);
+
 // Workspace layout of the backward pass (byte offsets, 256-aligned sections).
 struct BwdWorkspace {
   size_t dq_off, lse2_off, delta_off, total;

@@ -52,7 +52,8 @@ typedef enum {
   FA_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small */
   FA_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
   FA_ERR_DEVICE_TIMEOUT = 5,   /* a kernel's bounded wait ran out (device error word) */
-  FA_ERR_DEVICE_INTERNAL = 6   /* a kernel found its shared memory misaligned */
+  FA_ERR_DEVICE_INTERNAL = 6,  /* a kernel found its shared memory misaligned */
+  FA_ERR_SCRATCH_LIMIT = 7     /* flash_attn_bwd_noalloc: shape needs more than its fixed scratch */
 } fa_status;
 
 /*
@@ -101,6 +102,38 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
                          int B, int H, int N, int d, float scale, int causal,
                          const int32_t* kv_len, const uint8_t* block_mask,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward pass for callers that cannot allocate device memory. (The pages
+ * describing the method have no counterpart of this call; it is an interface
+ * convenience.) Some callers cannot provide the workspace flash_attn_bwd
+ * needs: a plug-in running inside another runtime's execute callback, where
+ * allocating device memory is not allowed; a serving loop that must never
+ * call cudaMalloc on the request path, because it synchronises the device
+ * and can stall every stream; a program whose device memory belongs to a
+ * pool that hands out no raw buffers. This call computes exactly what
+ * flash_attn_bwd computes (same arguments, minus the workspace) and takes
+ * its scratch from a fixed array of FA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * that the library keeps on every device that loads it, until the process
+ * exits. Neither it nor the library allocates anything.
+ *   - Shapes whose flash_attn_bwd_workspace_size exceeds
+ *     FA_BWD_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_SCRATCH_LIMIT
+ *     before anything is launched.
+ *   - All calls on a device share the one array. Calls ordered on one stream
+ *     are safe; calls whose kernels may overlap on the GPU (several streams,
+ *     or several host threads without ordering) race on it and give wrong
+ *     results. Each call rewrites whatever it reads from the array, so what a
+ *     previous call left there does not matter.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture
+ *     starts.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+fa_status flash_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                 int B, int H, int N, int d, float scale, int causal,
+                                 const int32_t* kv_len, const uint8_t* block_mask, void* stream);
 
 /*
  * The tile classifier the kernels use to decide which 128 x 128 tiles to
