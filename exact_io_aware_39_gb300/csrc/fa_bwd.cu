@@ -23,7 +23,8 @@
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
 //      dQ partials are added into an fp32 workspace with vector reductions.
 //      Warps: 0-3 recompute P and dS (thread = key row), 4-7 drain dQ from
-//      TMEM into the workspace (thread = query row), 8 TMA producer, 9 MMA.
+//      TMEM into the workspace (thread = query row), 8 TMA producer, 9 MMA,
+//      10-11 idle (their warpgroup hands its registers to warps 0-7).
 //   3. fa_bwd_dq:   dQ = bf16(scale * dQ_acc).
 #include "fa_common.cuh"
 #include "fa_ptx.cuh"
@@ -34,7 +35,11 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 384;
+// per-thread registers after reallocation: 128 x (232 + 184 + 88) = 384 x 168
+constexpr int kComputeRegs = 232;
+constexpr int kDrainRegs = 184;
+constexpr int kOtherRegs = 88;
 
 template <int D>
 struct BwdLayout {
@@ -140,6 +145,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t tS = tmem + 2u * D;
   const uint32_t tP = tmem + 2u * D + 128u;   // dP^T, then the dQ partial
 
+  if (warp >= 8) regs_dec<kOtherRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -239,6 +245,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ P and dS (thread = key row)
+    regs_inc<kComputeRegs>();
     const int r = tid;
     const int krow = kTile * kj + r;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -362,8 +369,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       bulk_commit_group();
       bulk_wait_group_all();
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
+    regs_inc<kDrainRegs>();
     const int r = tid - 128;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int i = next_live(0);

@@ -10,11 +10,13 @@
 // chip (milestone page, "The idea -- Recomputation").
 //
 // GB300 design (not the pages' A100 design):
-//   * one CTA owns two 128-row Q tiles of one (batch, head); 10 warps:
+//   * one CTA owns two 128-row Q tiles of one (batch, head); 12 warps:
 //       warps 0-3  softmax / correction / epilogue of Q tile 0 (TMEM lanes 0-127)
 //       warps 4-7  the same for Q tile 1
 //       warp  8    TMA producer (Q once, then a K ring and a V ring)
 //       warp  9    TMEM allocator and the single thread that issues tcgen05.mma
+//       warps 10-11 idle; the third warpgroup gives its registers to the
+//                  softmax warpgroups (216 vs 72 per thread)
 //   * S_t = Q_t K_j^T accumulates in TMEM (128 fp32 columns per Q tile); the
 //     softmax warps overwrite it in place with P_t as packed bf16, which the
 //     tensor core then reads straight from TMEM for O_t += P_t V_j;
@@ -36,7 +38,9 @@ namespace fa {
 
 namespace {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
+constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 registers
+constexpr int kOtherRegs = 72;
 constexpr int kListMax = kMaxN / kTile;   // union list capacity
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 
@@ -139,6 +143,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   const uint32_t tmem = misc[0];
   const int len = (int)misc[2];
 
+  if (warp >= 8) regs_dec<kOtherRegs>();
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -266,8 +271,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       mma_commit(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax groups
+    regs_inc<kSoftmaxRegs>();
     const int t = warp >> 2;                 // Q tile of this warpgroup
     const int r = tid & 127;                 // row within the tile = TMEM lane
     const int qi = qi0 + t;
@@ -313,9 +319,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
         }
       }
-      float mx = x[0];
+      float mx8[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+      for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = mx * sl2;
       // move the reference max only when the row max grew by more than the
       // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
@@ -340,7 +350,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         tmem_st_wait();
       }
       const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum = 0.f;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -348,13 +358,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2(fmaf(x[64 * hh + 2 * i], sl2, -ref));
           const float p1 = ex2(fmaf(x[64 * hh + 2 * i + 1], sl2, -ref));
-          sum += p0 + p1;
+          sum8[i & 7] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tS + 32u * hh, pk);
       }
       tmem_st_wait();
-      l += sum;
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tc_fence_before();
       mbar_arrive(bar(L::bPFull + t));
       ++n;

@@ -102,7 +102,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity. Returns false (after
 // reporting) on timeout or when another thread of the CTA has aborted.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t n = 0;
@@ -129,7 +129,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
 // Bounded wait that ignores the abort flag: used on exit paths to let copies
 // and MMAs that were already issued finish before shared memory or TMEM is
 // released.
-static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try(bar, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
@@ -313,6 +313,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Warpgroup register reallocation: every warp of a warpgroup executes the
+// same one. The counts of a kernel must add up to at most the registers it
+// was launched with (threads x registers per thread at launch).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
 }
 
 // ---------------------------------------------------------------------------
