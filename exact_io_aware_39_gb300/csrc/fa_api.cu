@@ -96,6 +96,19 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// 3-D view [BH, Np, d] of the fp32 dQ accumulator, box 32 x 128 x 1 (one
+// 128-byte row per box row), 128-byte swizzle.
+fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Np, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)Np * d * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status check_shape(int B, int H, int N, int d, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1 || !std::isfinite(scale) || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
@@ -134,6 +147,10 @@ int internal_device_error_word(unsigned int** err) {
 
 int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return make_map(m, base, BH, N, d);
+}
+
+int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, int d) {
+  return make_dq_map(m, dq_acc, BH, Np, d);
 }
 
 cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len, const uint8_t* block_mask,
@@ -213,6 +230,8 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
   if (make_map(&tq, Q, BH, N, d) || make_map(&tk, K, BH, N, d) || make_map(&tv, V, BH, N, d) ||
       make_map(&tdo, dO, BH, N, d) || make_map(&tdk, dK, BH, N, d) || make_map(&tdv, dV, BH, N, d))
     return FA_ERR_CUDA;
+  CUtensorMap tdq;
+  if (make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
   if (launch_bwd_pre(O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   BwdParams p{};
   p.kv_len = kv_len;
@@ -229,7 +248,7 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   const ProfileScope prof(s);
   prof.before();
-  const cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, p, s);
+  const cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   prof.after();
   if (e != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_dq(dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;

@@ -21,7 +21,10 @@
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
 //        dK  += dS^T Q         (A = dS^T from smem K-major, B = Q MN-major)
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
-//      dQ partials are added into an fp32 workspace with vector reductions.
+//      Each dQ partial is drained from TMEM into shared memory (the dS buffer,
+//      idle between the dQ MMA and the next dS) in two 64-column halves and
+//      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
+//      128-byte lines.
 //      Warps: 0-3 recompute P and dS (thread = key row), 4-7 drain dQ from
 //      TMEM into the workspace (thread = query row), 8 TMA producer, 9 MMA,
 //      10-11 idle (their warpgroup hands its registers to warps 0-7).
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
-                   const BwdParams p, const float scale) {
+                   const __grid_constant__ CUtensorMap tdq, const BwdParams p, const float scale) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -237,7 +240,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           mma_ss(tP, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bdQFull));
         mma_commit(bar(L::bQEmpty + s));
-        mma_commit(bar(L::bdSEmpty));
       }
       mma_commit(bar(L::bFinal));
       mma_commit(bar(L::bDrain));
@@ -371,28 +373,50 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
+    // TMEM -> fp32 rows in the dS buffer (two boxes of [128 rows x 32 fp32],
+    // 128-byte swizzled) -> TMA reduce-add into the accumulator, 64 columns
+    // at a time; the dS buffer is handed back to warps 0-3 afterwards.
     regs_inc<kDrainRegs>();
     const int r = tid - 128;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    uint8_t* stage = smem + L::kdS;
     int i = next_live(0);
     for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
+      // the dQ MMA (and the dK MMA before it) have completed: TMEM holds the
+      // partial and the dS buffer is no longer read by the tensor core
       if (!mbar_wait_warp(bar(L::bdQFull), (uint32_t)it & 1u, ctl, 130)) break;
       tc_fence_after();
-      float* dst = p.dq_acc + ((size_t)bh * Np + (size_t)kTile * i + r) * D;
-      uint32_t u[D / 32][32];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tP + lane_off + 32u * cc, u[cc]);
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tP + lane_off + 64u * half, u0);
+        tmem_ld32(tP + lane_off + 64u * half + 32u, u1);
+        tmem_ld_wait(u0);
+        tmem_ld_wait(u1);
+        if (half == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(L::bdQFree));   // the TMEM columns may be overwritten
+        }
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(u[cc]);
-      tc_fence_before();
-      mbar_arrive(bar(L::bdQFree));
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          red_add_v4(dst + 32 * cc + 4 * k, __uint_as_float(u[cc][4 * k]), __uint_as_float(u[cc][4 * k + 1]),
-                     __uint_as_float(u[cc][4 * k + 2]), __uint_as_float(u[cc][4 * k + 3]));
+        for (int k = 0; k < 8; ++k) {    // 8 chunks of 4 fp32 per 32-column box
+          const uint32_t sw = (uint32_t)(((k ^ (r & 7)) << 4) + (r >> 3) * 1024 + (r & 7) * 128);
+          *reinterpret_cast<uint4*>(stage + sw) = make_uint4(u0[4 * k], u0[4 * k + 1], u0[4 * k + 2], u0[4 * k + 3]);
+          *reinterpret_cast<uint4*>(stage + 16384 + sw) =
+              make_uint4(u1[4 * k], u1[4 * k + 1], u1[4 * k + 2], u1[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (r == 0) {
+          tma_reduce_add_3d(&tdq, smem_u32(stage), 64 * half, kTile * i, bh);
+          tma_reduce_add_3d(&tdq, smem_u32(stage) + 16384u, 64 * half + 32, kTile * i, bh);
+          bulk_commit_group();
+          bulk_wait_group_read_all();      // staging may be rewritten
+        }
+        named_bar_sync(2, 128);
+      }
+      if (r == 0) mbar_arrive(bar(L::bdSEmpty));
     }
+    if (r == 0) bulk_wait_group_all();     // reductions complete before exit
   }
 
   tc_fence_before();
@@ -471,7 +495,7 @@ __global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16
 template <int D>
 cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                              const BwdParams& p, float scale, cudaStream_t s) {
+                              const CUtensorMap& tdq, const BwdParams& p, float scale, cudaStream_t s) {
   using L = BwdLayout<D>;
   static bool configured = false;
   if (!configured) {
@@ -481,7 +505,7 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
     configured = true;
   }
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  fa_bwd_main_kernel<D><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p, scale);
+  fa_bwd_main_kernel<D><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
   return cudaGetLastError();
 }
 
@@ -506,10 +530,10 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, fl
 
 cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
-                            const BwdParams& p, cudaStream_t s) {
+                            const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   const float scale = p.scale_log2 / 1.4426950408889634f;
-  if (d == 64) return launch_bwd_main_d<64>(tq, tk, tv, tdo, tdk, tdv, p, scale, s);
-  return launch_bwd_main_d<128>(tq, tk, tv, tdo, tdk, tdv, p, scale, s);
+  if (d == 64) return launch_bwd_main_d<64>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
+  return launch_bwd_main_d<128>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
 }
 
 cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,

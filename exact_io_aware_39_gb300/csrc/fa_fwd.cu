@@ -48,31 +48,36 @@ template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // separate K and V rings; the K ring is the deeper one, since the S MMAs
+  // that read K come first
+  static constexpr int kStagesK = (D == 64) ? 6 : 3;
+  static constexpr int kStagesV = (D == 64) ? 5 : 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;   // 8-byte mbarriers
+  static constexpr int kV = kK + kStagesK * kTileBytes;
+  static constexpr int kBar = kV + kStagesV * kTileBytes;   // 8-byte mbarriers
   // barrier slots
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
-  static constexpr int bKEmpty = bKFull + kStages;
-  static constexpr int bVFull = bKEmpty + kStages;
-  static constexpr int bVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bVEmpty + kStages;    // [2]
+  static constexpr int bKEmpty = bKFull + kStagesK;
+  static constexpr int bVFull = bKEmpty + kStagesK;
+  static constexpr int bVEmpty = bVFull + kStagesV;
+  static constexpr int bSFull = bVEmpty + kStagesV;   // [2]
   static constexpr int bPFull = bSFull + 2;           // [2]
   static constexpr int bOFinal = bPFull + 2;          // [2]
   static constexpr int bDrain = bOFinal + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort, list length
-  static constexpr int kList = kMisc + 16;
-  static constexpr int kEnd = kList + 4 * kListMax;
-  static constexpr int kSmemBytes = kEnd + 1024;      // + alignment slack
+  static constexpr int kList = kMisc + 16;           // uint16 entries
+  static constexpr int kSmemBytes = kList + 2 * kListMax;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ int entry_j(uint32_t e) { return (int)(e & 0xFFFFu); }
-__device__ __forceinline__ uint32_t entry_live(uint32_t e, int t) { return (e >> (16 + t)) & 1u; }
-__device__ __forceinline__ uint32_t entry_partial(uint32_t e, int t) { return (e >> (18 + t)) & 1u; }
+// union-list entry: key tile j in bits 0-9 (j < 1024), live flags of the two
+// Q tiles in bits 10-11, partial flags in bits 12-13
+__device__ __forceinline__ int entry_j(uint32_t e) { return (int)(e & 0x3FFu); }
+__device__ __forceinline__ uint32_t entry_live(uint32_t e, int t) { return (e >> (10 + t)) & 1u; }
+__device__ __forceinline__ uint32_t entry_partial(uint32_t e, int t) { return (e >> (12 + t)) & 1u; }
 __device__ __forceinline__ uint32_t entry_nlive(uint32_t e) {
   return entry_live(e, 0) + entry_live(e, 1);
 }
@@ -83,8 +88,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
               const FwdParams p) {
   using L = FwdLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
   const int tid = threadIdx.x;
@@ -104,8 +108,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
-  uint32_t* list = reinterpret_cast<uint32_t*>(smem + L::kList);
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
   Ctl ctl{p.err, abort_flag};
+
+  if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
+    if (tid == 0) {
+      uint32_t dummy = 0;
+      Ctl c0{p.err, &dummy};
+      report_error(c0, kErrSmemAlign, 0);
+    }
+    return;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
@@ -126,12 +139,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       if (j < p.nT) {
         const int s0 = tile_state(qi0, j, kvl, p.nT, p.causal, p.block_mask);
         const int s1 = has_t1 ? tile_state(qi0 + 1, j, kvl, p.nT, p.causal, p.block_mask) : kSkip;
-        e = (uint32_t)j | ((s0 != kSkip) ? (1u << 16) : 0u) | ((s1 != kSkip) ? (1u << 17) : 0u) |
-            ((s0 == kPartial) ? (1u << 18) : 0u) | ((s1 == kPartial) ? (1u << 19) : 0u);
+        e = (uint32_t)j | ((s0 != kSkip) ? (1u << 10) : 0u) | ((s1 != kSkip) ? (1u << 11) : 0u) |
+            ((s0 == kPartial) ? (1u << 12) : 0u) | ((s1 == kPartial) ? (1u << 13) : 0u);
       }
-      const bool live = (e >> 16) & 3u;
+      const bool live = (e >> 10) & 3u;
       const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
-      if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = e;
+      if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
       count += __popc(ball);
     }
     if (lane == 0) misc[2] = (uint32_t)count;
@@ -158,28 +171,31 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                       kTile * (qi0 + t), bh);
       int nk = 0, nv = 0;   // K and V loads issued
       for (int e = 0; e < len; ++e) {
-        const int s = e % L::kStages;
-        const uint32_t n = (uint32_t)(e / L::kStages);
         const int j = entry_j(list[e]);
-        if (e >= L::kStages && !mbar_wait(bar(L::bKEmpty + s), (n - 1) & 1u, ctl, 1)) break;
-        mbar_arrive_expect_tx(bar(L::bKFull + s), L::kTileBytes);
+        const int sk = e % L::kStagesK;
+        const uint32_t nk_ = (uint32_t)(e / L::kStagesK);
+        if (e >= L::kStagesK && !mbar_wait(bar(L::bKEmpty + sk), (nk_ - 1) & 1u, ctl, 1)) break;
+        mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
         for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kK + s * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + s),
+          tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk),
                       64 * h, kTile * j, bh);
         ++nk;
-        if (e >= L::kStages && !mbar_wait(bar(L::bVEmpty + s), (n - 1) & 1u, ctl, 2)) break;
-        mbar_arrive_expect_tx(bar(L::bVFull + s), L::kTileBytes);
+        const int sv = e % L::kStagesV;
+        const uint32_t nv_ = (uint32_t)(e / L::kStagesV);
+        if (e >= L::kStagesV && !mbar_wait(bar(L::bVEmpty + sv), (nv_ - 1) & 1u, ctl, 2)) break;
+        mbar_arrive_expect_tx(bar(L::bVFull + sv), L::kTileBytes);
         for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kV + s * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + s),
+          tma_load_3d(sbase + L::kV + sv * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + sv),
                       64 * h, kTile * j, bh);
         ++nv;
       }
       // every load issued must have landed before the CTA may exit
       drain_wait(bar(L::bQFull), 0);
-      for (int s = 0; s < L::kStages; ++s) {
-        if (s < nk) drain_wait(bar(L::bKFull + s), (uint32_t)((s + ((nk - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
-        if (s < nv) drain_wait(bar(L::bVFull + s), (uint32_t)((s + ((nv - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
-      }
+      // the last load into stage s was entry s + S * floor((n - 1 - s) / S)
+      for (int s = 0; s < L::kStagesK && s < nk; ++s)
+        drain_wait(bar(L::bKFull + s), (uint32_t)((nk - 1 - s) / L::kStagesK) & 1u);
+      for (int s = 0; s < L::kStagesV && s < nv; ++s)
+        drain_wait(bar(L::bVFull + s), (uint32_t)((nv - 1 - s) / L::kStagesV) & 1u);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -190,8 +206,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
       const uint32_t sQ[2] = {sbase + L::kQ, sbase + L::kQ + L::kTileBytes};
       int pos[2], st[2], npv[2];
-      uint32_t kdone[L::kStages], vdone[L::kStages];
-      for (int s = 0; s < L::kStages; ++s) { kdone[s] = 0; vdone[s] = 0; }
+      uint32_t kdone[L::kStagesK], vdone[L::kStagesV];
+      for (int s = 0; s < L::kStagesK; ++s) kdone[s] = 0;
+      for (int s = 0; s < L::kStagesV; ++s) vdone[s] = 0;
       enum { kNeedS = 0, kNeedP = 1, kDone = 2 };
       for (int t = 0; t < 2; ++t) {
         int e = 0;
@@ -210,8 +227,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int t = 0; t < 2; ++t) {
           if (st[t] == kNeedS) {
             const int e = pos[t];
-            const int s = e % L::kStages;
-            const uint32_t ph = (uint32_t)(e / L::kStages) & 1u;
+            const int s = e % L::kStagesK;
+            const uint32_t ph = (uint32_t)(e / L::kStagesK) & 1u;
             if (mbar_test(bar(L::bKFull + s), ph)) {
               tc_fence_after();
               const uint32_t sK = sbase + L::kK + s * L::kTileBytes;
@@ -228,8 +245,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
           } else if (st[t] == kNeedP) {
             const int e = pos[t];
-            const int s = e % L::kStages;
-            const uint32_t ph = (uint32_t)(e / L::kStages) & 1u;
+            const int s = e % L::kStagesV;
+            const uint32_t ph = (uint32_t)(e / L::kStagesV) & 1u;
             if (mbar_test(bar(L::bPFull + t), (uint32_t)npv[t] & 1u) &&
                 mbar_test(bar(L::bVFull + s), ph)) {
               tc_fence_after();

@@ -160,6 +160,22 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src,
       :: "l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1), "r"(c2) : "memory");
 }
 
+// Element-wise reduce-add of a shared-memory box into global memory through
+// the tensor map (fp32 add performed in L2 by the TMA unit).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src,
+                                                  int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      :: "l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+// Wait until the shared-memory sources of all committed bulk groups have
+// been read (the buffers may be rewritten; the global writes may still be
+// in flight).
+__device__ __forceinline__ void bulk_wait_group_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
