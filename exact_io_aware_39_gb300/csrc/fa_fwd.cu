@@ -13,9 +13,10 @@
 //   * one CTA owns two 128-row Q tiles of one (batch, head); 12 warps:
 //       warps 0-3  softmax / correction / epilogue of Q tile 0 (TMEM lanes 0-127)
 //       warps 4-7  the same for Q tile 1
-//       warp  8    TMA producer (Q once, then a K ring and a V ring)
+//       warp  8    TMA producer of Q (once) and of the K ring
 //       warp  9    TMEM allocator and the single thread that issues tcgen05.mma
-//       warps 10-11 idle; the third warpgroup gives its registers to the
+//       warp 10    TMA producer of the V ring
+//       warp 11    idle; the third warpgroup gives its registers to the
 //                  softmax warpgroups (216 vs 72 per thread)
 //   * S_t = Q_t K_j^T accumulates in TMEM (128 fp32 columns per Q tile); the
 //     softmax warps overwrite it in place with P_t as packed bf16, which the
@@ -158,18 +159,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   if (warp >= 8) regs_dec<kOtherRegs>();
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
       tma_prefetch_map(&tq);
       tma_prefetch_map(&tk);
-      tma_prefetch_map(&tv);
       const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
       mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
       for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
         for (int h = 0; h < L::kHalves; ++h)
           tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
                       kTile * (qi0 + t), bh);
-      int nk = 0, nv = 0;   // K and V loads issued
+      int nk = 0;   // K loads issued
       for (int e = 0; e < len; ++e) {
         const int j = entry_j(list[e]);
         const int sk = e % L::kStagesK;
@@ -180,6 +180,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk),
                       64 * h, kTile * j, bh);
         ++nk;
+      }
+      // every load issued must have landed before the CTA may exit; the last
+      // load into stage s was entry s + S * floor((n - 1 - s) / S)
+      drain_wait(bar(L::bQFull), 0);
+      for (int s = 0; s < L::kStagesK && s < nk; ++s)
+        drain_wait(bar(L::bKFull + s), (uint32_t)((nk - 1 - s) / L::kStagesK) & 1u);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ V producer
+    // (its own thread, so that the K ring can run ahead of the V ring)
+    if (lane == 0) {
+      tma_prefetch_map(&tv);
+      int nv = 0;   // V loads issued
+      for (int e = 0; e < len; ++e) {
+        const int j = entry_j(list[e]);
         const int sv = e % L::kStagesV;
         const uint32_t nv_ = (uint32_t)(e / L::kStagesV);
         if (e >= L::kStagesV && !mbar_wait(bar(L::bVEmpty + sv), (nv_ - 1) & 1u, ctl, 2)) break;
@@ -189,99 +204,84 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                       64 * h, kTile * j, bh);
         ++nv;
       }
-      // every load issued must have landed before the CTA may exit
-      drain_wait(bar(L::bQFull), 0);
-      // the last load into stage s was entry s + S * floor((n - 1 - s) / S)
-      for (int s = 0; s < L::kStagesK && s < nk; ++s)
-        drain_wait(bar(L::bKFull + s), (uint32_t)((nk - 1 - s) / L::kStagesK) & 1u);
       for (int s = 0; s < L::kStagesV && s < nv; ++s)
         drain_wait(bar(L::bVFull + s), (uint32_t)((nv - 1 - s) / L::kStagesV) & 1u);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Fixed schedule over the union list: at entry e, for each Q tile t, first
+    // the pending O_t += P_t V of t's previous live entry (waiting for P_t),
+    // then S_t = Q_t K_e^T if t is live at e. For dense rows this is
+    //   PV0(e-1), S0(e), PV1(e-1), S1(e), PV0(e), ...
+    // so that while one softmax group works the tensor core runs the other
+    // tile's products. A pending PV is issued at the very next entry, so each
+    // V slot is released one entry after its load and the K slot of entry e
+    // right after its S products.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
       const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
-      const uint32_t sQ[2] = {sbase + L::kQ, sbase + L::kQ + L::kTileBytes};
-      int pos[2], st[2], npv[2];
-      uint32_t kdone[L::kStagesK], vdone[L::kStagesV];
-      for (int s = 0; s < L::kStagesK; ++s) kdone[s] = 0;
-      for (int s = 0; s < L::kStagesV; ++s) vdone[s] = 0;
-      enum { kNeedS = 0, kNeedP = 1, kDone = 2 };
-      for (int t = 0; t < 2; ++t) {
-        int e = 0;
-        while (e < len && !entry_live(list[e], t)) ++e;
-        pos[t] = e;
-        st[t] = (e < len) ? kNeedS : kDone;
-        npv[t] = 0;
-      }
+      const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
+      const uint64_t dK0 = desc_kmajor(sbase + L::kK, 0);
+      const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
+      constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
+      int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
+      uint32_t npv[2] = {0u, 0u};   // PV groups issued per Q tile
       bool ok = mbar_wait(bar(L::bQFull), 0, ctl, 4);
       tc_fence_after();
-      uint64_t idle_t0 = globaltimer();
-      uint32_t idle = 0;
-      while (ok && (st[0] != kDone || st[1] != kDone)) {
-        bool progressed = false;
+
+      // O_t += P_t V_{entry pe}
+      auto issue_pv = [&](int t, int pe) -> bool {
+        const int sv = pe % L::kStagesV;
+        if (!mbar_wait(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
+        if (!mbar_wait(bar(L::bVFull + sv), (uint32_t)(pe / L::kStagesV) & 1u, ctl, 6)) return false;
+        tc_fence_after();
+        const uint64_t dV = dV0 + (uint64_t)sv * kSlotStep;
+        const uint32_t acc0 = npv[t] > 0 ? 1u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ts(tO[t], tS[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
+        ++npv[t];
+        return true;
+      };
+
+      for (int e = 0; e < len && ok; ++e) {
+        const uint32_t ent = list[e];
+        const int sk = e % L::kStagesK;
+        bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (st[t] == kNeedS) {
-            const int e = pos[t];
-            const int s = e % L::kStagesK;
-            const uint32_t ph = (uint32_t)(e / L::kStagesK) & 1u;
-            if (mbar_test(bar(L::bKFull + s), ph)) {
+          if (!ok) break;
+          if (prev[t] >= 0) {
+            ok = issue_pv(t, prev[t]);
+            prev[t] = -1;
+            if (!ok) break;
+          }
+          if (entry_live(ent, t)) {
+            if (!k_ready) {
+              ok = mbar_wait(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
+              if (!ok) break;
               tc_fence_after();
-              const uint32_t sK = sbase + L::kK + s * L::kTileBytes;
-#pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks)
-                mma_ss(tS[t], desc_kmajor(sQ[t], ks), desc_kmajor(sK, ks), idS, ks > 0 ? 1u : 0u);
-              mma_commit(bar(L::bSFull + t));
-              if (++kdone[s] == entry_nlive(list[e])) {
-                kdone[s] = 0;
-                mma_commit(bar(L::bKEmpty + s));
-              }
-              st[t] = kNeedP;
-              progressed = true;
+              k_ready = true;
             }
-          } else if (st[t] == kNeedP) {
-            const int e = pos[t];
-            const int s = e % L::kStagesV;
-            const uint32_t ph = (uint32_t)(e / L::kStagesV) & 1u;
-            if (mbar_test(bar(L::bPFull + t), (uint32_t)npv[t] & 1u) &&
-                mbar_test(bar(L::bVFull + s), ph)) {
-              tc_fence_after();
-              const uint32_t sV = sbase + L::kV + s * L::kTileBytes;
+            const uint64_t dK = dK0 + (uint64_t)sk * kSlotStep;
 #pragma unroll
-              for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ts(tO[t], tS[t] + (uint32_t)ks * 8u, desc_mnmajor(sV, ks), idO,
-                       (npv[t] > 0 || ks > 0) ? 1u : 0u);
-              ++npv[t];
-              if (++vdone[s] == entry_nlive(list[e])) {
-                vdone[s] = 0;
-                mma_commit(bar(L::bVEmpty + s));
-              }
-              int n = e + 1;
-              while (n < len && !entry_live(list[n], t)) ++n;
-              pos[t] = n;
-              if (n < len) {
-                st[t] = kNeedS;
-              } else {
-                mma_commit(bar(L::bOFinal + t));
-                st[t] = kDone;
-              }
-              progressed = true;
-            }
+            for (int ks = 0; ks < D / 16; ++ks)
+              mma_ss(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
+            mma_commit(bar(L::bSFull + t));
+            prev[t] = e;
           }
         }
-        if (progressed) {
-          idle = 0;
-          idle_t0 = globaltimer();
-        } else if ((++idle & 63u) == 0u) {
-          if (*abort_flag) break;
-          if (globaltimer() - idle_t0 > kWaitLimitNs) {
-            report_error(ctl, kErrTimeout, 5);
-            break;
-          }
+        if (!ok) break;
+        mma_commit(bar(L::bKEmpty + sk));                       // K_e is no longer needed
+        if (e > 0) mma_commit(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
+      }
+      if (ok) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
+          if (ok && npv[t] > 0) mma_commit(bar(L::bOFinal + t));
         }
       }
       // every MMA this thread issued must be complete before TMEM is freed

@@ -217,14 +217,17 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
+// D[tmem] (+)= A[smem desc] * B[smem desc]. The MMA touches no memory the
+// compiler tracks, so the statement carries no memory clobber (a clobber
+// would force reloads around every MMA on the single issuing thread); volatile
+// asm statements keep their order relative to the barrier and commit ones.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]
@@ -234,7 +237,7 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive once on the mbarrier when every tcgen05 operation this thread has
@@ -278,6 +281,15 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kstep) {
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kstep) {
   return sdesc_sw128(tile + (uint32_t)kstep * 2048u, 16384u, 1024u);
 }
+
+// Per-step descriptor increments (in the 16-byte units of the address
+// field) for the layouts above, so that a loop can add a constant to a base
+// descriptor computed once: K-major step k -> atom k / 4 (16 KB) plus 32 bytes
+// per step inside the atom; MN-major step k -> 2048 bytes.
+__host__ __device__ constexpr uint64_t kmajor_step(int kstep) {
+  return (uint64_t)((kstep >> 2) * 1024 + (kstep & 3) * 2);
+}
+__host__ __device__ constexpr uint64_t mnmajor_step(int kstep) { return (uint64_t)(kstep * 128); }
 
 // TMEM loads/stores: 32 lanes x 32 bits, 32 consecutive columns per thread.
 #define FA_R32(a) a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[8], a[9], a[10], a[11], \
