@@ -48,7 +48,7 @@ template <int D>
 struct BwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = (D == 64) ? 3 : 2;   // Q/dO ring depth (smem-limited at d = 128)
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;                  // [stages]
@@ -124,7 +124,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdQFree) ? 128u : 1u);
+      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdQFree) ? 4u : 1u);   // 4 = warps
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -299,7 +299,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::bPFull));
+      mbar_arrive_warp(bar(L::bPFull));
 
       // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> bf16 -> swizzled smem
       if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)it & 1u, ctl, 122))) break;
@@ -326,7 +326,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(L::bdSFull));
+      mbar_arrive_warp(bar(L::bdSFull));
     }
 
     // epilogue: dV and scale * dK for every key row of the tile (zeros when
@@ -395,7 +395,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         tmem_ld_wait(u1);
         if (half == D / 64 - 1) {
           tc_fence_before();
-          mbar_arrive(bar(L::bdQFree));   // the TMEM columns may be overwritten
+          mbar_arrive_warp(bar(L::bdQFree));   // the TMEM columns may be overwritten
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {    // 8 chunks of 4 fp32 per 32-column box

@@ -123,7 +123,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 128u : 1u);
+      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 4u : 1u);   // 4 = warps
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -383,7 +383,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       tmem_st_wait();
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       tc_fence_before();
-      mbar_arrive(bar(L::bPFull + t));
+      mbar_arrive_warp(bar(L::bPFull + t));
       ++n;
     }
 

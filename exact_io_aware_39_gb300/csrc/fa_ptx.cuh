@@ -78,6 +78,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// One arrival per warp: the warp's lanes synchronise (which orders their
+// earlier memory and, after tcgen05.fence::before_thread_sync, TMEM accesses)
+// and lane 0 arrives. Barriers signalled this way count warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0u) mbar_arrive(bar);
+}
+
 // Non-blocking test of phase completion.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
