@@ -21,6 +21,8 @@
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
 //        dK  += dS^T Q         (A = dS^T from smem K-major, B = Q MN-major)
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
+//      S^T of the next query tile is issued after dK and dQ of the current one,
+//      which leaves its Q load the longest window.
 //      Each dQ partial is drained from TMEM into shared memory (the dS buffer,
 //      idle between the dQ MMA and the next dS) in two 64-column halves and
 //      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
@@ -218,17 +220,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
           mma_ts(tdV, tS + (uint32_t)ks * 8u, desc_mnmajor(sdO, ks), idV, (it > 0 || ks > 0) ? 1u : 0u);
-        // next S^T, overlapping the dS computation of this tile
-        if (it + 1 < len) {
-          const int s1 = (it + 1) % L::kStages;
-          if (!(ok = mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114))) break;
-          tc_fence_after();
-          const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
-          mma_commit(bar(L::bSFull));
-        }
         // dK += dS^T Q ; dQ_i = dS K
         if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)it & 1u, ctl, 115))) break;
         tc_fence_after();
@@ -240,6 +231,18 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           mma_ss(tP, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bdQFull));
         mma_commit(bar(L::bQEmpty + s));
+        // next S^T (after this tile's dK and dQ: a longer window for its Q load)
+        if (it + 1 < len) {
+          const int s1 = (it + 1) % L::kStages;
+          if (!(ok = mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114))) break;
+          tc_fence_after();
+          const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
+          mma_commit(bar(L::bSFull));
+        }
+
       }
       mma_commit(bar(L::bFinal));
       mma_commit(bar(L::bDrain));
