@@ -239,6 +239,7 @@ def run_ours(args):
     from exact_io_aware_39_gb300 import build as _build
     from exact_io_aware_39_gb300.flops import attention_flops
     from exact_io_aware_39_gb300.inputs import WORKLOADS, make_case
+    from exact_io_aware_39_gb300.replicas import job_throughput, max_over_ranks
     fa.load(_build.build() if rank == 0 or world == 1 else _build.LIB_PATH)
 
     w = WORKLOADS[args.workload]
@@ -315,12 +316,8 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error during timing: {detail}")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * flop_step * K / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(total_ms, dev)
+    value = job_throughput(flop_step, K, world, total_ms)
     clocks = sampler.stop() if sampler else None
 
     # end-to-end through the public API with pinned host buffers
@@ -353,13 +350,8 @@ def run_ours(args):
             e2e_step()
         eb.record(stream)
         barrier()
-        e2e_ms = ea.elapsed_time(eb)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * flop_step * Ke / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(ea.elapsed_time(eb), dev)
+        e2e = {"value": job_throughput(flop_step, Ke, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / Ke}
 
