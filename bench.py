@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--workload", default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="element type of Q, K, V, dO (and of the outputs)")
     ap.add_argument("--shape", default=None,
                     help="B,H,N override of the workload (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -247,7 +249,7 @@ def run_ours(args):
         import dataclasses
         sb, sh, sn = (int(x) for x in args.shape.split(","))
         w = dataclasses.replace(w, B=sb, H=sh, N=sn, name=f"{w.name}@{sb}x{sh}x{sn}")
-    c = make_case(w)
+    c = make_case(w, dtype=torch.float16 if args.dtype == "f16" else torch.bfloat16)
     B, H, N, d = c["B"], c["H"], c["N"], c["d"]
     kv_np = None if c["kv_len"] is None else c["kv_len"].numpy()
     bm_np = None if c["block_mask"] is None else c["block_mask"].numpy()
@@ -409,7 +411,7 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic N(0,1) bf16, seeded (no dataset)",
             "config": _workload_config(w, {
                 "l2": "L2 flushed between steps" if flush else "inputs larger than L2 (not flushed)",

@@ -6,15 +6,15 @@ in-place build script, the seeded synthetic inputs and FLOP accounting.
 Importing the package does not load the library; the first call does, and
 raises if it is missing.
 """
-from ._lib import (FlashAttnError, attention_bwd, attention_fwd, device_error,
-                   flash_attn_bwd, flash_attn_bwd_noalloc, flash_attn_bwd_workspace_size, flash_attn_fwd,
+from ._lib import (FlashAttnError, attention_bwd, attention_fwd, device_error, fa_options,
+                   flash_attn_bwd, flash_attn_bwd_ex, flash_attn_bwd_noalloc, flash_attn_fwd_ex, flash_attn_bwd_workspace_size, flash_attn_fwd,
                    flash_attn_get_device_error, flash_attn_set_profile_events,
                    flash_attn_status_string, flash_attn_tile_map, flash_attn_version, load,
                    profile_next_call, tile_map)
 
 __all__ = [
-    "FlashAttnError", "attention_bwd", "attention_fwd", "device_error", "flash_attn_bwd",
-    "flash_attn_bwd_noalloc",
+    "FlashAttnError", "attention_bwd", "attention_fwd", "device_error", "fa_options", "flash_attn_bwd",
+    "flash_attn_bwd_ex", "flash_attn_bwd_noalloc", "flash_attn_fwd_ex",
     "flash_attn_bwd_workspace_size", "flash_attn_fwd", "flash_attn_get_device_error",
     "flash_attn_set_profile_events", "flash_attn_status_string", "flash_attn_tile_map",
     "flash_attn_version", "load", "profile_next_call", "tile_map",

@@ -24,11 +24,23 @@ BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # every symbol include/flash_attn.h declares
 EXPORTS = [
-    "flash_attn_fwd", "flash_attn_bwd_workspace_size", "flash_attn_bwd", "flash_attn_bwd_noalloc",
+    "flash_attn_fwd", "flash_attn_fwd_ex", "flash_attn_bwd_workspace_size", "flash_attn_bwd",
+    "flash_attn_bwd_ex", "flash_attn_bwd_noalloc",
     "flash_attn_tile_map",
     "flash_attn_get_device_error", "flash_attn_set_profile_events", "flash_attn_status_string",
     "flash_attn_version",
 ]
+
+
+FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1
+
+
+class fa_options(ctypes.Structure):
+    """Mirror of the C struct fa_options (size must be set)."""
+    _fields_ = [("size", ctypes.c_uint32), ("dtype", ctypes.c_int32)]
+
+    def __init__(self, dtype=FA_DTYPE_BF16):
+        super().__init__(ctypes.sizeof(fa_options), dtype)
 
 
 class FlashAttnError(RuntimeError):
@@ -51,6 +63,11 @@ def load(path=LIB_PATH):
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.flash_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, vp]
     lib.flash_attn_fwd.restype = i32
+    opt_p = ctypes.POINTER(fa_options)
+    lib.flash_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, opt_p, vp]
+    lib.flash_attn_fwd_ex.restype = i32
+    lib.flash_attn_bwd_ex.argtypes = [vp] * 9 + [i32, i32, i32, i32, f32, i32, vp, vp, opt_p, vp, sz, vp]
+    lib.flash_attn_bwd_ex.restype = i32
     lib.flash_attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.flash_attn_bwd_workspace_size.restype = sz
     lib.flash_attn_bwd.argtypes = [vp] * 9 + [i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]
@@ -77,6 +94,18 @@ def load(path=LIB_PATH):
 
 def flash_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, stream):
     return load().flash_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, stream)
+
+
+def flash_attn_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, options, stream):
+    return load().flash_attn_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask,
+                                    None if options is None else ctypes.byref(options), stream)
+
+
+def flash_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, block_mask,
+                      options, workspace, workspace_bytes, stream):
+    return load().flash_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len,
+                                    block_mask, None if options is None else ctypes.byref(options),
+                                    workspace, workspace_bytes, stream)
 
 
 def flash_attn_bwd_workspace_size(B, H, N, d):
@@ -140,15 +169,20 @@ def _check(st, where):
 
 
 def _check_inputs(*ts):
+    """Validates the tensors and returns the fa_options for their dtype."""
     import torch
     for t in ts:
         if t is None:
             continue
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("tensors must be contiguous CUDA tensors")
-    for t in ts[:3]:
-        if t.dtype != torch.bfloat16 or t.dim() != 4:
-            raise ValueError("Q, K, V must be bfloat16 [B, H, N, d]")
+    dt = ts[0].dtype
+    if dt not in (torch.bfloat16, torch.float16):
+        raise ValueError("Q, K, V must be bfloat16 or float16 [B, H, N, d]")
+    for t in ts:
+        if t is not None and (t.dtype != dt or t.dim() != 4):
+            raise ValueError("Q, K, V (and O, dO) must share one 16-bit dtype and be [B, H, N, d]")
+    return fa_options(FA_DTYPE_F16 if dt == torch.float16 else FA_DTYPE_BF16)
 
 
 def _mask_args(kv_len, block_mask):
@@ -164,14 +198,14 @@ def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, ou
                   stream=None):
     """O, LSE = attention(q, k, v) on the GPU. q, k, v: bf16 [B, H, N, d]."""
     import torch
-    _check_inputs(q, k, v)
+    opts = _check_inputs(q, k, v)
     B, H, N, d = q.shape
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     kv_p, bm_p = _mask_args(kv_len, block_mask)
-    st = flash_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, float(scale),
-                        int(bool(causal)), kv_p, bm_p, _stream(stream))
-    _check(st, "flash_attn_fwd")
+    st = flash_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, float(scale),
+                           int(bool(causal)), kv_p, bm_p, opts, _stream(stream))
+    _check(st, "flash_attn_fwd_ex")
     return o, l
 
 
@@ -179,7 +213,7 @@ def attention_bwd(q, k, v, o, do, lse, scale, causal=False, kv_len=None, block_m
                   workspace=None, dq=None, dk=None, dv=None, stream=None):
     """dQ, dK, dV of attention on the GPU (recomputing S and P on chip)."""
     import torch
-    _check_inputs(q, k, v, o, do)
+    opts = _check_inputs(q, k, v, o, do)
     B, H, N, d = q.shape
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -188,10 +222,10 @@ def attention_bwd(q, k, v, o, do, lse, scale, causal=False, kv_len=None, block_m
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     kv_p, bm_p = _mask_args(kv_len, block_mask)
-    st = flash_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                        _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), kv_p, bm_p,
-                        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "flash_attn_bwd")
+    st = flash_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                           _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), kv_p, bm_p, opts,
+                           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "flash_attn_bwd_ex")
     return dq, dk, dv
 
 

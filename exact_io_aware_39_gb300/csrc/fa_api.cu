@@ -83,14 +83,15 @@ fa_status device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D view [BH, N, d] of a bf16 tensor, box 64 x 128 x 1, 128-byte swizzle;
-// rows past N read as zeros and are not written by stores.
-fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+// 3-D view [BH, N, d] of a bf16 (or fp16) tensor, box 64 x 128 x 1, 128-byte
+// swizzle; rows past N read as zeros and are not written by stores.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool f16 = false) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -107,6 +108,21 @@ fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+struct Options {
+  bool f16 = false;
+};
+
+// Reads the caller's options (NULL = defaults). Fields beyond the caller's
+// declared size keep their defaults, so older callers of a grown struct work.
+fa_status read_options(const fa_options* opt, Options* out) {
+  *out = Options{};
+  if (opt == nullptr) return FA_OK;
+  if (opt->size < sizeof(uint32_t) + sizeof(int32_t)) return FA_ERR_INVALID_ARG;
+  if (opt->dtype != FA_DTYPE_BF16 && opt->dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  out->f16 = opt->dtype == FA_DTYPE_F16;
+  return FA_OK;
 }
 
 fa_status check_shape(int B, int H, int N, int d, float scale, int causal) {
@@ -167,11 +183,13 @@ using namespace fa;
 
 extern "C" {
 
-fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
-                         int d, float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
-                         void* stream) {
+fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                            int N, int d, float scale, int causal, const int32_t* kv_len,
+                            const uint8_t* block_mask, const fa_options* options, void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, causal);
   if (st != FA_OK) return st;
+  Options o;
+  if ((st = read_options(options, &o)) != FA_OK) return st;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return FA_ERR_INVALID_ARG;
@@ -179,8 +197,8 @@ fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, f
   if ((st = device_state(&ds)) != FA_OK) return st;
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
-  if (make_map(&tq, Q, BH, N, d) || make_map(&tk, K, BH, N, d) || make_map(&tv, V, BH, N, d) ||
-      make_map(&to, O, BH, N, d))
+  if (make_map(&tq, Q, BH, N, d, o.f16) || make_map(&tk, K, BH, N, d, o.f16) ||
+      make_map(&tv, V, BH, N, d, o.f16) || make_map(&to, O, BH, N, d, o.f16))
     return FA_ERR_CUDA;
   FwdParams p{};
   p.lse = LSE;
@@ -195,9 +213,15 @@ fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, f
   p.scale_log2 = scale * 1.4426950408889634f;
   const ProfileScope prof(static_cast<cudaStream_t>(stream));
   prof.before();
-  const cudaError_t e = launch_fwd(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_fwd(d, o.f16, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   prof.after();
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                         int d, float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
+                         void* stream) {
+  return flash_attn_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, nullptr, stream);
 }
 
 size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d) {
@@ -205,12 +229,14 @@ size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d) {
   return bwd_workspace_layout(B, H, N, d).total;
 }
 
-fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                         const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
-                         int causal, const int32_t* kv_len, const uint8_t* block_mask, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                            const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                            float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
+                            const fa_options* options, void* workspace, size_t workspace_bytes, void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, causal);
   if (st != FA_OK) return st;
+  Options o;
+  if ((st = read_options(options, &o)) != FA_OK) return st;
   const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
   for (const void* q : ptrs)
     if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
@@ -227,12 +253,13 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
   float* delta = reinterpret_cast<float*>(ws + w.delta_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (make_map(&tq, Q, BH, N, d) || make_map(&tk, K, BH, N, d) || make_map(&tv, V, BH, N, d) ||
-      make_map(&tdo, dO, BH, N, d) || make_map(&tdk, dK, BH, N, d) || make_map(&tdv, dV, BH, N, d))
+  if (make_map(&tq, Q, BH, N, d, o.f16) || make_map(&tk, K, BH, N, d, o.f16) ||
+      make_map(&tv, V, BH, N, d, o.f16) || make_map(&tdo, dO, BH, N, d, o.f16) ||
+      make_map(&tdk, dK, BH, N, d, o.f16) || make_map(&tdv, dV, BH, N, d, o.f16))
     return FA_ERR_CUDA;
   CUtensorMap tdq;
   if (make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
-  if (launch_bwd_pre(O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_pre(o.f16, O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   BwdParams p{};
   p.kv_len = kv_len;
   p.block_mask = block_mask;
@@ -248,11 +275,19 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   const ProfileScope prof(s);
   prof.before();
-  const cudaError_t e = launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
+  const cudaError_t e = launch_bwd_main(d, o.f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
   prof.after();
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_bwd_dq(dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_dq(o.f16, dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                         const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
+                         int causal, const int32_t* kv_len, const uint8_t* block_mask, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return flash_attn_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, block_mask,
+                           nullptr, workspace, workspace_bytes, stream);
 }
 
 fa_status flash_attn_tile_map(int B, int N, int causal, const int32_t* kv_len, const uint8_t* block_mask,

@@ -84,7 +84,7 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
   return (uint32_t)(h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4) + ((col & 7) << 1));
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -190,10 +190,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && len > 0) {
-      constexpr uint32_t idSP = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idV = idesc_bf16(128, D, false, true);
-      constexpr uint32_t idK = idesc_bf16(128, D, false, true);
-      constexpr uint32_t idQ = idesc_bf16(128, D, true, true);
+      constexpr uint32_t idSP = idesc_16<F16>(128, 128, false, false);
+      constexpr uint32_t idV = idesc_16<F16>(128, D, false, true);
+      constexpr uint32_t idK = idesc_16<F16>(128, D, false, true);
+      constexpr uint32_t idQ = idesc_16<F16>(128, D, true, true);
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdS = sbase + L::kdS;
       bool ok = mbar_wait(bar(L::bKV), 0, ctl, 110) && mbar_wait(bar(L::bQFull), 0, ctl, 111);
       if (ok) {
@@ -297,7 +297,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(x[64 * hh + 2 * c], x[64 * hh + 2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack2<F16>(x[64 * hh + 2 * c], x[64 * hh + 2 * c + 1]);
         tmem_st32(tS + lane_off + 32u * hh, pk);
       }
       tmem_st_wait();
@@ -319,7 +319,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const int c0 = 32 * cc + 2 * c;
           const float d0 = x[c0] * (__uint_as_float(u[2 * c]) - dlt[c0]);
           const float d1 = x[c0 + 1] * (__uint_as_float(u[2 * c + 1]) - dlt[c0 + 1]);
-          pk[c] = pack_bf16x2(d0, d1);
+          pk[c] = pack2<F16>(d0, d1);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -356,7 +356,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
+          pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k);
@@ -433,8 +433,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 // D = rowsum(dO * O) (fp32), LSE2 = LSE * log2(e) with +inf for -inf and
 // padding rows, dQ accumulator zeroed. One group of d/8 threads per row, each
 // owning 8 consecutive columns.
-template <int D>
-__global__ void fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+template <int D, bool F16>
+__global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                   const float* __restrict__ lse, float* __restrict__ dq_acc,
                                   float* __restrict__ lse2, float* __restrict__ delta, int BH, int N, int Np) {
   constexpr int G = D / 8;   // threads per row
@@ -449,12 +449,11 @@ __global__ void fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __n
     const size_t off = ((size_t)bh * N + n) * D + part * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(o + off);
     const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float2 af = __bfloat1622float2(a2[k]);
-      const float2 gf = __bfloat1622float2(g2[k]);
+      const float2 af = unpack2<F16>(aw[k]);
+      const float2 gf = unpack2<F16>(gw[k]);
       acc = fmaf(af.x, gf.x, acc);
       acc = fmaf(af.y, gf.y, acc);
     }
@@ -475,8 +474,8 @@ __global__ void fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __n
   }
 }
 
-template <int D>
-__global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, float scale,
+template <int D, bool F16>
+__global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, float scale,
                                  int BH, int N, int Np) {
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one thread per 8 columns
   const long long total = (long long)BH * N * (D / 8);
@@ -488,68 +487,85 @@ __global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16
   const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Np + n) * D + part * 8);
   const float4 a = src[0], c = src[1];
   uint4 out;
-  out.x = pack_bf16x2(a.x * scale, a.y * scale);
-  out.y = pack_bf16x2(a.z * scale, a.w * scale);
-  out.z = pack_bf16x2(c.x * scale, c.y * scale);
-  out.w = pack_bf16x2(c.z * scale, c.w * scale);
+  out.x = pack2<F16>(a.x * scale, a.y * scale);
+  out.y = pack2<F16>(a.z * scale, a.w * scale);
+  out.z = pack2<F16>(c.x * scale, c.y * scale);
+  out.w = pack2<F16>(c.z * scale, c.w * scale);
   *reinterpret_cast<uint4*>(dq + (size_t)row * D + part * 8) = out;
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                               const CUtensorMap& tdq, const BwdParams& p, float scale, cudaStream_t s) {
   using L = BwdLayout<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  fa_bwd_main_kernel<D><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
+  fa_bwd_main_kernel<D, F16><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
   return cudaGetLastError();
+}
+
+template <int D, bool F16>
+void launch_bwd_pre_d(const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
+                      float* delta, int BH, int N, int Np, cudaStream_t s) {
+  const long long threads = (long long)BH * Np * (D / 8);
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  fa_bwd_pre_kernel<D, F16><<<grid, block, 0, s>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                                   lse, dq_acc, lse2, delta, BH, N, Np);
+}
+
+template <int D, bool F16>
+void launch_bwd_dq_d(const float* dq_acc, void* dq, float scale, int BH, int N, int Np, cudaStream_t s) {
+  const long long threads = (long long)BH * N * (D / 8);
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  fa_bwd_dq_kernel<D, F16><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np);
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
+cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
                            float* delta, int BH, int N, int nT, int d, cudaStream_t s) {
   const int Np = nT * kTile;
-  const long long threads = (long long)BH * Np * (d / 8);
-  const int block = 256;
-  const unsigned grid = (unsigned)((threads + block - 1) / block);
-  if (d == 64)
-    fa_bwd_pre_kernel<64><<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                static_cast<const __nv_bfloat16*>(dout), lse, dq_acc, lse2,
-                                                delta, BH, N, Np);
-  else
-    fa_bwd_pre_kernel<128><<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                 static_cast<const __nv_bfloat16*>(dout), lse, dq_acc, lse2,
-                                                 delta, BH, N, Np);
+  if (f16) {
+    if (d == 64) launch_bwd_pre_d<64, true>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
+    else launch_bwd_pre_d<128, true>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
+  } else {
+    if (d == 64) launch_bwd_pre_d<64, false>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
+    else launch_bwd_pre_d<128, false>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   const float scale = p.scale_log2 / 1.4426950408889634f;
-  if (d == 64) return launch_bwd_main_d<64>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
-  return launch_bwd_main_d<128>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
+  if (f16)
+    return d == 64 ? launch_bwd_main_d<64, true>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s)
+                   : launch_bwd_main_d<128, true>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
+  return d == 64 ? launch_bwd_main_d<64, false>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s)
+                 : launch_bwd_main_d<128, false>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
 }
 
-cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
+cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
                           cudaStream_t s) {
   const int Np = nT * kTile;
-  const long long threads = (long long)BH * N * (d / 8);
-  if (threads == 0) return cudaSuccess;
-  const int block = 256;
-  const unsigned grid = (unsigned)((threads + block - 1) / block);
-  if (d == 64)
-    fa_bwd_dq_kernel<64><<<grid, block, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, BH, N, Np);
-  else
-    fa_bwd_dq_kernel<128><<<grid, block, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), scale, BH, N, Np);
+  if ((long long)BH * N == 0) return cudaSuccess;
+  if (f16) {
+    if (d == 64) launch_bwd_dq_d<64, true>(dq_acc, dq, scale, BH, N, Np, s);
+    else launch_bwd_dq_d<128, true>(dq_acc, dq, scale, BH, N, Np, s);
+  } else {
+    if (d == 64) launch_bwd_dq_d<64, false>(dq_acc, dq, scale, BH, N, Np, s);
+    else launch_bwd_dq_d<128, false>(dq_acc, dq, scale, BH, N, Np, s);
+  }
   return cudaGetLastError();
 }
 

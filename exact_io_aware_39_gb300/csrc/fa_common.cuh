@@ -64,22 +64,23 @@ struct BwdParams {
 
 // Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1,
 // 128-byte swizzle. Return the cudaError_t of the launch.
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+// f16 selects fp16 elements (else bf16) for Q, K, V, O, dO, dQ, dK, dV.
+cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
 
-cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* dq_acc,
+cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const float* lse, float* dq_acc,
                            float* lse2, float* delta, int BH, int N, int nT, int d,
                            cudaStream_t s);
 
 // tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 128 x 1,
 // 128-byte swizzle (internal_make_dq_map); partial dQ tiles are added into it
 // with TMA reduce-add.
-cudaError_t launch_bwd_main(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tdq,
                             const BwdParams& p, cudaStream_t s);
 
-cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
+cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
                           cudaStream_t s);
 
 cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len,
@@ -88,7 +89,7 @@ cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_
 // Host helpers defined with the C ABI (return fa_status values).
 int internal_check_shape(int B, int H, int N, int d, float scale, int causal);
 int internal_device_error_word(unsigned int** err);   // current device; runs its set-up once
-int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d);
+int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d);   // bf16
 int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, int d);
 
 // Workspace layout of the backward pass (byte offsets, 256-aligned sections).

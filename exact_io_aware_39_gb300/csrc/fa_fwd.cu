@@ -83,7 +83,7 @@ __device__ __forceinline__ uint32_t entry_nlive(uint32_t e) {
   return entry_live(e, 0) + entry_live(e, 1);
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -218,8 +218,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     // V slot is released one entry after its load and the K slot of entry e
     // right after its S products.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
+      constexpr uint32_t idO = idesc_16<F16>(128, D, false, true);
       const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
       const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
       const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
@@ -376,7 +376,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           const float p0 = ex2(fmaf(x[64 * hh + 2 * i], sl2, -ref));
           const float p1 = ex2(fmaf(x[64 * hh + 2 * i + 1], sl2, -ref));
           sum8[i & 7] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          pk[i] = pack2<F16>(p0, p1);
         }
         tmem_st32(tS + 32u * hh, pk);
       }
@@ -410,7 +410,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
+          pk[i] = pack2<F16>(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
         // 32 columns = 4 chunks of 16 bytes, 128B-swizzled rows
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -445,29 +445,29 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   using L = FwdLayout<D>;
   static bool configured = false;   // per process; the attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));
-  fa_fwd_kernel<D><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
+  fa_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, p, s);
-  return launch_fwd_d<128>(tq, tk, tv, to, p, s);
+  if (f16) return d == 64 ? launch_fwd_d<64, true>(tq, tk, tv, to, p, s) : launch_fwd_d<128, true>(tq, tk, tv, to, p, s);
+  return d == 64 ? launch_fwd_d<64, false>(tq, tk, tv, to, p, s) : launch_fwd_d<128, false>(tq, tk, tv, to, p, s);
 }
 
 }  // namespace fa

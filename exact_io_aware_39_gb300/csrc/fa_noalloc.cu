@@ -93,7 +93,7 @@ extern "C" fa_status flash_attn_bwd_noalloc(const void* Q, const void* K, const 
   CUtensorMap tdq;
   if (internal_make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
   // the pre-pass zeroes the dQ accumulator and rewrites both row vectors
-  if (launch_bwd_pre(O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_pre(false, O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   BwdParams p{};
   p.kv_len = kv_len;
   p.block_mask = block_mask;
@@ -107,7 +107,7 @@ extern "C" fa_status flash_attn_bwd_noalloc(const void* Q, const void* K, const 
   p.nT = nT;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  if (launch_bwd_main(d, tq, tk, tv, tdo, tdk, tdv, tdq, p, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_bwd_dq(dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_main(d, false, tq, tk, tv, tdo, tdk, tdv, tdq, p, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_dq(false, dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -264,6 +264,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A and B of one 16-bit type: bf16 (format 1) or fp16 (format 0).
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_mn) {
+  return F16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16(M, N, a_mn, b_mn);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle. Fields: [0,14) start
 // address >> 4, [16,30) leading byte offset >> 4, [32,46) stride byte offset
 // >> 4, [46,48) = 1 (descriptor version), [49,52) base offset (0: every
@@ -377,6 +383,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two floats -> one 32-bit word of the kernel's 16-bit element type (low half
+// = first element), round to nearest even.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+// One 32-bit word of two 16-bit elements -> two floats (exact).
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if (F16) {
+    float2 r;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "r"(w));
+    return r;
+  }
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {

@@ -64,14 +64,15 @@ def n_tiles(N: int) -> int:
     return (N + TILE - 1) // TILE
 
 
-def draw_qkvdo(B, H, N, d, seed=0):
-    """Q, K, V, dO as bfloat16 CPU tensors [B, H, N, d], drawn in that order."""
+def draw_qkvdo(B, H, N, d, seed=0, dtype=torch.bfloat16):
+    """Q, K, V, dO as 16-bit CPU tensors [B, H, N, d] (bfloat16 unless dtype
+    says otherwise), drawn in that order."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     out = []
     for _ in range(4):
         t = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
-        out.append(t.to(torch.bfloat16))
+        out.append(t.to(dtype))
     return tuple(out)
 
 
@@ -91,7 +92,7 @@ def draw_block_mask(N, p, seed=2):
     return m
 
 
-def make_case(w: Workload, seed=0, B=None, H=None, N=None):
+def make_case(w: Workload, seed=0, B=None, H=None, N=None, dtype=torch.bfloat16):
     """All inputs of one workload (optionally with B, H or N overridden).
 
     Returns a dict of CPU tensors: q, k, v, do (bf16), kv_len (int32 [B] or
@@ -100,7 +101,7 @@ def make_case(w: Workload, seed=0, B=None, H=None, N=None):
     B = w.B if B is None else B
     H = w.H if H is None else H
     N = w.N if N is None else N
-    q, k, v, do = draw_qkvdo(B, H, N, w.d, seed)
+    q, k, v, do = draw_qkvdo(B, H, N, w.d, seed, dtype)
     kv_len = None
     if w.kv_len_range is not None:
         lo, hi = w.kv_len_range

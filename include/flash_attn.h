@@ -12,7 +12,8 @@
  * Conventions shared by every call
  * --------------------------------
  *  - Tensors are row-major, contiguous, one (batch, head) after another:
- *      Q, K, V, O, dO, dQ, dK, dV : bfloat16 [B, H, N, d]
+ *      Q, K, V, O, dO, dQ, dK, dV : bfloat16 [B, H, N, d] (fp16 through the
+ *                                   *_ex calls)
  *      LSE                         : float32  [B, H, N]
  *    N is the sequence length of both queries and keys. d is 64 or 128.
  *  - Every pointer named here is a DEVICE pointer of the current CUDA device,
@@ -57,6 +58,23 @@ typedef enum {
 } fa_status;
 
 /*
+ * Options of the *_ex calls (no counterpart on the pages; the pages name
+ * FP16 and BF16 as the formats the method is meant for -- Flash Attention
+ * glossary, "Tensor Cores"; pixelation.org article, "Actionable Next Steps").
+ * size must be set to sizeof(fa_options) by the caller; fields past the size
+ * a caller declares keep their defaults, so the struct can grow without
+ * breaking older callers. Passing NULL for the options selects all defaults.
+ *   dtype: element type of Q, K, V, O, dO, dQ, dK, dV: FA_DTYPE_BF16
+ *          (default) or FA_DTYPE_F16. LSE stays fp32.
+ */
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_F16 = 1 } fa_dtype;
+
+typedef struct {
+  uint32_t size;
+  int32_t dtype;
+} fa_options;
+
+/*
  * Forward pass. Computes, for every (b, h) and query row i,
  *   O[b,h,i,:]  = sum_j P_ij V[b,h,j,:],  P_ij = exp(S_ij - LSE[b,h,i]),
  *   LSE[b,h,i]  = ln sum_j exp(S_ij),     S_ij = scale * Q[b,h,i,:] . K[b,h,j,:]
@@ -72,6 +90,13 @@ typedef enum {
 fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                          int B, int H, int N, int d, float scale, int causal,
                          const int32_t* kv_len, const uint8_t* block_mask, void* stream);
+
+/* flash_attn_fwd with options (see fa_options); flash_attn_fwd is this call
+ * with options = NULL. */
+fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t* kv_len, const uint8_t* block_mask,
+                            const fa_options* options, void* stream);
 
 /*
  * Bytes of device workspace flash_attn_bwd needs for this shape (fp32 dQ
@@ -102,6 +127,16 @@ fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void
                          int B, int H, int N, int d, float scale, int causal,
                          const int32_t* kv_len, const uint8_t* block_mask,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* flash_attn_bwd with options (see fa_options); the options must match the
+ * forward call that produced O and LSE. flash_attn_bwd is this call with
+ * options = NULL. */
+fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t* kv_len, const uint8_t* block_mask,
+                            const fa_options* options, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /*
  * Backward pass for callers that cannot allocate device memory. (The pages

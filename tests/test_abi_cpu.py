@@ -79,3 +79,16 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert L.flash_attn_bwd(*args, p, ws - 1, None) == 3          # too small
     assert L.flash_attn_bwd(*args, bad, ws, None) == 3            # misaligned
     assert L.flash_attn_bwd(*args, None, ws, None) == 3           # missing
+
+
+def test_options_validated_before_any_launch(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    p = ctypes.c_void_p(1 << 20)
+    bad_dtype = L.fa_options(7)
+    assert L.flash_attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, bad_dtype, None) == 2
+    short = L.fa_options(0)
+    short.size = 2
+    assert L.flash_attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, short, None) == 1
+    ws = L.flash_attn_bwd_workspace_size(1, 1, 128, 64)
+    args = [p] * 9 + [1, 1, 128, 64, 0.1, 0, None, None]
+    assert L.flash_attn_bwd_ex(*args, bad_dtype, p, ws, None) == 2

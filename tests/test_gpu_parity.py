@@ -103,9 +103,9 @@ SMALL = [
 ]
 
 
-def _small_case(name, B, H, N, d, causal, kv, bm):
+def _small_case(name, B, H, N, d, causal, kv, bm, dtype=torch.bfloat16):
     w = Workload(name, B, H, N, d, causal, 1.0 / math.sqrt(d))
-    c = make_case(w, seed=zlib.crc32(name.encode()) % 1000)
+    c = make_case(w, seed=zlib.crc32(name.encode()) % 1000, dtype=dtype)
     if kv is not None:
         c["kv_len"] = torch.tensor(kv, dtype=torch.int32)
     nT = (N + 127) // 128
@@ -140,6 +140,30 @@ def test_tile_map_bit_exact(fa, spec):
     got = fa.tile_map(c["B"], c["N"], c["causal"], kv, bm).cpu().numpy()
     want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
     assert np.array_equal(got, want)
+
+
+FP16 = [s for s in SMALL if s[0] in ("tiny_noncausal", "ragged_causal", "d128_causal_ragged",
+                                      "kv_len_mixed", "block_mask_causal_d128", "all_masks")]
+
+
+@pytest.mark.parametrize("spec", FP16, ids=[s[0] for s in FP16])
+def test_fp16_matches_oracle(fa, spec):
+    """The fp16 element type (fa_options.dtype = FA_DTYPE_F16): same kernels,
+    same tolerances."""
+    c = _small_case(*spec, dtype=torch.float16)
+    got = _run_gpu(fa, c)
+    ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], c["scale"], c["causal"],
+                                   c["kv_len"], c["block_mask"])
+    _compare(got, ref)
+
+
+def test_fp16_long_causal_sampled_heads(fa):
+    w = WORKLOADS["long_causal"]
+    c = make_case(w, dtype=torch.float16)
+    got = _run_gpu(fa, c)
+    heads = [(0, 5), (0, 20)]
+    ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], w.scale, w.causal, heads=heads)
+    _compare(got, ref, heads=heads)
 
 
 # heads compared per workload: all where the oracle is quick, else a sample
