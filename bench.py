@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--workload", default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--p-drop", type=float, default=0.0,
+                    help="dropout probability on P (0 = none); the mask is regenerated in the backward pass")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="element type of Q, K, V, dO (and of the outputs)")
     ap.add_argument("--shape", default=None,
@@ -268,9 +270,11 @@ def run_ours(args):
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     stream = torch.cuda.current_stream()
 
+    pd = dict(p_drop=args.p_drop, seed=1234)
+
     def step():
-        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse)
-        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv)
+        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse, **pd)
+        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv, **pd)
 
     def barrier():
         if world > 1:
@@ -302,9 +306,9 @@ def run_ours(args):
         e = ev[i]
         e[0].record(stream)
         fa.profile_next_call(e[1], e[2])
-        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse)
+        fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm, out=o, lse=lse, **pd)
         fa.profile_next_call(e[3], e[4])
-        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv)
+        fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm, workspace=ws, dq=dq, dk=dk, dv=dv, **pd)
         e[5].record(stream)
     barrier()
     wall1 = time.perf_counter()
@@ -356,9 +360,9 @@ def run_ours(args):
                     stream.wait_event(ev_down[i - 2])      # output slot downloaded
                 gq, gk, gv, gdo = g_in[sl]
                 go, gl, gdq, gdk, gdv = g_out[sl]
-                fa.attention_fwd(gq, gk, gv, w.scale, w.causal, kv, bm, out=go, lse=gl)
+                fa.attention_fwd(gq, gk, gv, w.scale, w.causal, kv, bm, out=go, lse=gl, **pd)
                 fa.attention_bwd(gq, gk, gv, go, gdo, gl, w.scale, w.causal, kv, bm, workspace=ws,
-                                 dq=gdq, dk=gdk, dv=gdv)
+                                 dq=gdq, dk=gdk, dv=gdv, **pd)
                 ev_comp[i].record(stream)
                 with torch.cuda.stream(down):
                     down.wait_event(ev_comp[i])
@@ -416,7 +420,8 @@ def run_ours(args):
             "config": _workload_config(w, {
                 "l2": "L2 flushed between steps" if flush else "inputs larger than L2 (not flushed)",
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "flop_per_step": flop_step, "fwd_flop": f_fwd, "bwd_flop": f_bwd}),
+                "flop_per_step": flop_step, "fwd_flop": f_fwd, "bwd_flop": f_bwd,
+                "p_drop": args.p_drop}),
             "pct_of_peak": 100.0 * value / world / peak,
             "gpu_launches": 4 * K,
             "timed_wall_s": wall1 - wall0,

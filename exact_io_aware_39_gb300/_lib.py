@@ -36,11 +36,12 @@ FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1
 
 
 class fa_options(ctypes.Structure):
-    """Mirror of the C struct fa_options (size must be set)."""
-    _fields_ = [("size", ctypes.c_uint32), ("dtype", ctypes.c_int32)]
+    """Mirror of the C struct fa_options (size is set by the constructor)."""
+    _fields_ = [("size", ctypes.c_uint32), ("dtype", ctypes.c_int32), ("p_drop", ctypes.c_float),
+                ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64)]
 
-    def __init__(self, dtype=FA_DTYPE_BF16):
-        super().__init__(ctypes.sizeof(fa_options), dtype)
+    def __init__(self, dtype=FA_DTYPE_BF16, p_drop=0.0, seed=0):
+        super().__init__(ctypes.sizeof(fa_options), dtype, float(p_drop), 0, int(seed))
 
 
 class FlashAttnError(RuntimeError):
@@ -195,10 +196,12 @@ def _mask_args(kv_len, block_mask):
 
 
 def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, out=None, lse=None,
-                  stream=None):
-    """O, LSE = attention(q, k, v) on the GPU. q, k, v: bf16 [B, H, N, d]."""
+                  stream=None, p_drop=0.0, seed=0):
+    """O, LSE = attention(q, k, v) on the GPU. q, k, v: bf16 or fp16 [B, H, N, d];
+    p_drop > 0 applies dropout to P (mask from Philox4x32-10 keyed by seed)."""
     import torch
     opts = _check_inputs(q, k, v)
+    opts.p_drop, opts.seed = float(p_drop), int(seed)
     B, H, N, d = q.shape
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -210,10 +213,12 @@ def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, ou
 
 
 def attention_bwd(q, k, v, o, do, lse, scale, causal=False, kv_len=None, block_mask=None,
-                  workspace=None, dq=None, dk=None, dv=None, stream=None):
-    """dQ, dK, dV of attention on the GPU (recomputing S and P on chip)."""
+                  workspace=None, dq=None, dk=None, dv=None, stream=None, p_drop=0.0, seed=0):
+    """dQ, dK, dV of attention on the GPU (recomputing S, P and the dropout
+    mask on chip); p_drop and seed must match the forward call."""
     import torch
     opts = _check_inputs(q, k, v, o, do)
+    opts.p_drop, opts.seed = float(p_drop), int(seed)
     B, H, N, d = q.shape
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk

@@ -5,6 +5,7 @@
 #include "fa_common.cuh"
 
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -112,6 +113,7 @@ fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) 
 
 struct Options {
   bool f16 = false;
+  DropoutParams drop{0u, 0u, 0u, 1.0f};
 };
 
 // Reads the caller's options (NULL = defaults). Fields beyond the caller's
@@ -122,6 +124,16 @@ fa_status read_options(const fa_options* opt, Options* out) {
   if (opt->size < sizeof(uint32_t) + sizeof(int32_t)) return FA_ERR_INVALID_ARG;
   if (opt->dtype != FA_DTYPE_BF16 && opt->dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
   out->f16 = opt->dtype == FA_DTYPE_F16;
+  if (opt->size >= offsetof(fa_options, seed) + sizeof(uint64_t)) {
+    const float p = opt->p_drop;
+    if (!std::isfinite(p) || p < 0.f || p >= 1.f) return FA_ERR_INVALID_ARG;
+    const uint32_t t = (uint32_t)std::floor((double)p * 256.0 + 0.5);
+    if (t > 255u) return FA_ERR_INVALID_ARG;
+    out->drop.t = t;
+    out->drop.keep_scale = (float)(256.0 / (256.0 - (double)t));
+    out->drop.seed_lo = (uint32_t)(opt->seed & 0xFFFFFFFFull);
+    out->drop.seed_hi = (uint32_t)(opt->seed >> 32);
+  }
   return FA_OK;
 }
 
@@ -211,6 +223,7 @@ fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O
   p.nT = (N + kTile - 1) / kTile;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.drop = o.drop;
   const ProfileScope prof(static_cast<cudaStream_t>(stream));
   prof.before();
   const cudaError_t e = launch_fwd(d, o.f16, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
@@ -273,6 +286,7 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
   p.nT = nT;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.drop = o.drop;
   const ProfileScope prof(s);
   prof.before();
   const cudaError_t e = launch_bwd_main(d, o.f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);

@@ -84,7 +84,7 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
   return (uint32_t)(h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4) + ((col & 7) << 1));
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -293,11 +293,38 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int c = 0; c < 128; ++c)
           if ((p.causal && krow > q0 + c) || krow >= kvl) x[c] = 0.f;
       }
+      // dropout: keep bits of the 128 query columns of this key row; one
+      // generator call (counter (query / 4, key / 4, bh, 0)) covers 4 queries,
+      // byte key mod 4 of each of its 4 words
+      uint32_t keep[4] = {0u, 0u, 0u, 0u};
+      if constexpr (DROP) {
+        const uint32_t qb0 = 32u * (uint32_t)i;
+        const uint32_t sh = 8u * ((uint32_t)krow & 3u);
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          const uint4 w = philox4x32_10(qb0 + (uint32_t)m, (uint32_t)krow >> 2, (uint32_t)bh, 0u,
+                                        p.drop.seed_lo, p.drop.seed_hi);
+          const uint32_t bits = (((w.x >> sh) & 0xFFu) >= p.drop.t ? 1u : 0u) |
+                                (((w.y >> sh) & 0xFFu) >= p.drop.t ? 2u : 0u) |
+                                (((w.z >> sh) & 0xFFu) >= p.drop.t ? 4u : 0u) |
+                                (((w.w >> sh) & 0xFFu) >= p.drop.t ? 8u : 0u);
+          keep[m >> 3] |= bits << (4 * (m & 7));
+        }
+      }
+      auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
+      // the dV operand is the dropped P (P * Z * keep_scale)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack2<F16>(x[64 * hh + 2 * c], x[64 * hh + 2 * c + 1]);
+        for (int c = 0; c < 32; ++c) {
+          const int c0 = 64 * hh + 2 * c;
+          if constexpr (DROP)
+            pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
+                               kept(c0 + 1) ? x[c0 + 1] * p.drop.keep_scale : 0.f);
+          else
+            pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
+        }
         tmem_st32(tS + lane_off + 32u * hh, pk);
       }
       tmem_st_wait();
@@ -317,8 +344,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int c0 = 32 * cc + 2 * c;
-          const float d0 = x[c0] * (__uint_as_float(u[2 * c]) - dlt[c0]);
-          const float d1 = x[c0 + 1] * (__uint_as_float(u[2 * c + 1]) - dlt[c0 + 1]);
+          float g0 = __uint_as_float(u[2 * c]), g1 = __uint_as_float(u[2 * c + 1]);
+          if constexpr (DROP) {   // dP = (dO V^T) * Z * keep_scale
+            g0 = kept(c0) ? g0 * p.drop.keep_scale : 0.f;
+            g1 = kept(c0 + 1) ? g1 * p.drop.keep_scale : 0.f;
+          }
+          const float d0 = x[c0] * (g0 - dlt[c0]);
+          const float d1 = x[c0 + 1] * (g1 - dlt[c0 + 1]);
           pk[c] = pack2<F16>(d0, d1);
         }
 #pragma unroll
@@ -494,20 +526,20 @@ __global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __r
   *reinterpret_cast<uint4*>(dq + (size_t)row * D + part * 8) = out;
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                               const CUtensorMap& tdq, const BwdParams& p, float scale, cudaStream_t s) {
   using L = BwdLayout<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  fa_bwd_main_kernel<D, F16><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
+  fa_bwd_main_kernel<D, F16, DROP><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
   return cudaGetLastError();
 }
 
@@ -548,11 +580,20 @@ cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtens
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   const float scale = p.scale_log2 / 1.4426950408889634f;
-  if (f16)
-    return d == 64 ? launch_bwd_main_d<64, true>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s)
-                   : launch_bwd_main_d<128, true>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
-  return d == 64 ? launch_bwd_main_d<64, false>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s)
-                 : launch_bwd_main_d<128, false>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
+  const bool drop = p.drop.t > 0;
+#define FA_BWD_CASE(DD, FF, DR) \
+  if (d == DD && f16 == FF && drop == DR) \
+    return launch_bwd_main_d<DD, FF, DR>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
+  FA_BWD_CASE(64, false, false)
+  FA_BWD_CASE(128, false, false)
+  FA_BWD_CASE(64, true, false)
+  FA_BWD_CASE(128, true, false)
+  FA_BWD_CASE(64, false, true)
+  FA_BWD_CASE(128, false, true)
+  FA_BWD_CASE(64, true, true)
+  FA_BWD_CASE(128, true, true)
+#undef FA_BWD_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,

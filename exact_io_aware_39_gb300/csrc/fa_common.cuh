@@ -40,6 +40,16 @@ __host__ __device__ __forceinline__ int effective_kv_len(const int32_t* kv_len, 
   return v < 0 ? 0 : (v > N ? N : v);
 }
 
+// Dropout on P. The keep decision of (batch-head bh, query i, key j) is the
+// byte 4 (i mod 4) + (j mod 4) of Philox4x32-10 with counter
+// (i / 4, j / 4, bh, 0) and key (seed_lo, seed_hi), compared with t: kept when
+// >= t, a kept value is multiplied by keep_scale = 256 / (256 - t).
+struct DropoutParams {
+  uint32_t seed_lo, seed_hi;
+  uint32_t t;          // 0..255; 0 keeps everything
+  float keep_scale;
+};
+
 struct FwdParams {
   float* lse;                 // [BH, N] fp32
   const int32_t* kv_len;      // [B] or null
@@ -48,6 +58,7 @@ struct FwdParams {
   int B, H, N, nT;
   int causal;
   float scale_log2;           // scale * log2(e)
+  DropoutParams drop;
 };
 
 struct BwdParams {
@@ -60,11 +71,13 @@ struct BwdParams {
   int B, H, N, nT;
   int causal;
   float scale_log2;
+  DropoutParams drop;
 };
 
 // Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1,
 // 128-byte swizzle. Return the cudaError_t of the launch.
 // f16 selects fp16 elements (else bf16) for Q, K, V, O, dO, dQ, dK, dV.
+// dropout is applied when p.drop.t > 0.
 cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
 

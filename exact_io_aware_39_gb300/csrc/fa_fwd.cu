@@ -83,7 +83,7 @@ __device__ __forceinline__ uint32_t entry_nlive(uint32_t e) {
   return entry_live(e, 0) + entry_live(e, 1);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -368,6 +368,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       }
       const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
       float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
+      // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4
+      const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
+      uint32_t rw = 0;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -375,8 +379,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2(fmaf(x[64 * hh + 2 * i], sl2, -ref));
           const float p1 = ex2(fmaf(x[64 * hh + 2 * i + 1], sl2, -ref));
-          sum8[i & 7] += p0 + p1;
-          pk[i] = pack2<F16>(p0, p1);
+          sum8[i & 7] += p0 + p1;   // the statistics use the undropped P
+          if constexpr (DROP) {
+            if ((i & 1) == 0)
+              rw = uint4_word(philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1),
+                                            (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi),
+                              (uint32_t)row & 3u);
+            const uint32_t sh = 16u * (uint32_t)(i & 1);
+            const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
+            const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
+            pk[i] = pack2<F16>(d0, d1);
+          } else {
+            pk[i] = pack2<F16>(p0, p1);
+          }
         }
         tmem_st32(tS + 32u * hh, pk);
       }
@@ -445,20 +460,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   using L = FwdLayout<D>;
   static bool configured = false;   // per process; the attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));
-  fa_fwd_kernel<D, F16><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
+  fa_fwd_kernel<D, F16, DROP><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -466,8 +481,19 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
-  if (f16) return d == 64 ? launch_fwd_d<64, true>(tq, tk, tv, to, p, s) : launch_fwd_d<128, true>(tq, tk, tv, to, p, s);
-  return d == 64 ? launch_fwd_d<64, false>(tq, tk, tv, to, p, s) : launch_fwd_d<128, false>(tq, tk, tv, to, p, s);
+  const bool drop = p.drop.t > 0;
+#define FA_FWD_CASE(DD, FF, DR) \
+  if (d == DD && f16 == FF && drop == DR) return launch_fwd_d<DD, FF, DR>(tq, tk, tv, to, p, s);
+  FA_FWD_CASE(64, false, false)
+  FA_FWD_CASE(128, false, false)
+  FA_FWD_CASE(64, true, false)
+  FA_FWD_CASE(128, true, false)
+  FA_FWD_CASE(64, false, true)
+  FA_FWD_CASE(128, false, true)
+  FA_FWD_CASE(64, true, true)
+  FA_FWD_CASE(128, true, true)
+#undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

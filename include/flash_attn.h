@@ -64,14 +64,28 @@ typedef enum {
  * size must be set to sizeof(fa_options) by the caller; fields past the size
  * a caller declares keep their defaults, so the struct can grow without
  * breaking older callers. Passing NULL for the options selects all defaults.
- *   dtype: element type of Q, K, V, O, dO, dQ, dK, dV: FA_DTYPE_BF16
- *          (default) or FA_DTYPE_F16. LSE stays fp32.
+ *   dtype:  element type of Q, K, V, O, dO, dQ, dK, dV: FA_DTYPE_BF16
+ *           (default) or FA_DTYPE_F16. LSE stays fp32.
+ *   p_drop: dropout probability applied to P between the two products, as
+ *           in the method's fused kernel (milestone page, "The idea");
+ *           0 (default) = none, otherwise in (0, 1) and used in steps of
+ *           1/256: t = round(256 p_drop) must be <= 255.
+ *   seed:   key of the dropout generator. Element (i, j) of batch-head
+ *           bh = b * H + h is kept when byte 4 (i mod 4) + (j mod 4) of
+ *           Philox4x32-10 with counter (i / 4, j / 4, bh, 0) and key
+ *           (seed mod 2^32, seed / 2^32) is >= t; kept values are scaled by
+ *           256 / (256 - t). The softmax statistics (LSE) use the undropped
+ *           P. The backward call regenerates the same mask from the same
+ *           p_drop and seed; nothing of the mask is stored.
  */
 typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_F16 = 1 } fa_dtype;
 
 typedef struct {
-  uint32_t size;
+  uint32_t size;      /* sizeof(fa_options) */
   int32_t dtype;
+  float p_drop;
+  uint32_t reserved;  /* 0 */
+  uint64_t seed;
 } fa_options;
 
 /*
