@@ -27,9 +27,10 @@
 //      idle between the dQ MMA and the next dS) in two 64-column halves and
 //      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
 //      128-byte lines.
-//      Warps: 0-3 recompute P and dS (thread = key row), 4-7 drain dQ from
-//      TMEM into the workspace (thread = query row), 8 TMA producer, 9 MMA,
-//      10-11 idle (their warpgroup hands its registers to warps 0-7).
+//      Warps: 0-3 and 4-7 recompute P and dS for query columns 0-63 and
+//      64-127 (thread = key row), 8-11 drain dQ from TMEM into the workspace
+//      (thread = query row), 12 TMA producer, 13 MMA, 14-15 idle (their
+//      warpgroup hands its registers to the others).
 //   3. fa_bwd_dq:   dQ = bf16(scale * dQ_acc).
 #include "fa_common.cuh"
 #include "fa_ptx.cuh"
@@ -40,11 +41,13 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 384;
-// per-thread registers after reallocation: 128 x (232 + 184 + 88) = 384 x 168
-constexpr int kComputeRegs = 232;
-constexpr int kDrainRegs = 184;
-constexpr int kOtherRegs = 88;
+constexpr int kBwdThreads = 512;
+// per-thread registers after reallocation: 128 x (160 + 160 + 112 + 80) = 512 x 128
+constexpr int kComputeRegs = 160;
+constexpr int kDrainRegs = 112;
+constexpr int kOtherRegs = 80;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 
 template <int D>
 struct BwdLayout {
@@ -126,15 +129,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdQFree) ? 4u : 1u);   // 4 = warps
+      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u : (i == L::bdQFree ? 4u : 1u));   // warps
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     int count = 0;
     for (int i = 0; i < p.nT; ++i) count += tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) != kSkip;
     misc[2] = (uint32_t)count;
@@ -150,8 +153,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t tS = tmem + 2u * D;
   const uint32_t tP = tmem + 2u * D + 128u;   // dP^T, then the dQ partial
 
-  if (warp >= 8) regs_dec<kOtherRegs>();
-  if (warp == 8) {
+  if (warp >= 12) regs_dec<kOtherRegs>();
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&tq);
@@ -187,7 +190,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           drain_wait(bar(L::bQFull + s),
                      (uint32_t)((s + ((nq - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && len > 0) {
       constexpr uint32_t idSP = idesc_16<F16>(128, 128, false, false);
@@ -219,7 +222,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts(tdV, tS + (uint32_t)ks * 8u, desc_mnmajor(sdO, ks), idV, (it > 0 || ks > 0) ? 1u : 0u);
+          // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
+          mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sdO, ks), idV,
+                 (it > 0 || ks > 0) ? 1u : 0u);
         // dK += dS^T Q ; dQ_i = dS K
         if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)it & 1u, ctl, 115))) break;
         tc_fence_after();
@@ -248,12 +253,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mma_commit(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P and dS (thread = key row)
+    // warpgroup cw handles query columns 64 cw .. 64 cw + 63 of each tile
     regs_inc<kComputeRegs>();
-    const int r = tid;
+    const int cw = warp >> 2;
+    const int cb = 64 * cw;
+    const int r = tid & 127;
     const int krow = kTile * kj + r;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
     int i = next_live(0);
@@ -263,45 +271,39 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 120))) break;
       if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)it & 1u, ctl, 121))) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024);
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
       const float* dlt = lse2 + kTile;
-      float x[128];
+      float x[64];
       {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
-        tmem_ld32(tS + lane_off + 0u, u0);
-        tmem_ld32(tS + lane_off + 32u, u1);
-        tmem_ld32(tS + lane_off + 64u, u2);
-        tmem_ld32(tS + lane_off + 96u, u3);
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tS + lane_off + (uint32_t)cb, u0);
+        tmem_ld32(tS + lane_off + (uint32_t)cb + 32u, u1);
         tmem_ld_wait(u0);
         tmem_ld_wait(u1);
-        tmem_ld_wait(u2);
-        tmem_ld_wait(u3);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           x[c] = __uint_as_float(u0[c]);
           x[32 + c] = __uint_as_float(u1[c]);
-          x[64 + c] = __uint_as_float(u2[c]);
-          x[96 + c] = __uint_as_float(u3[c]);
         }
       }
       // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
 #pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = ex2(fmaf(x[c], sl2, -lse2[c]));
+      for (int c = 0; c < 64; ++c) x[c] = ex2(fmaf(x[c], sl2, -lse2[c]));
       if (partial) {
-        const int q0 = kTile * i;
+        const int q0 = kTile * i + cb;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 64; ++c)
           if ((p.causal && krow > q0 + c) || krow >= kvl) x[c] = 0.f;
       }
-      // dropout: keep bits of the 128 query columns of this key row; one
-      // generator call (counter (query / 4, key / 4, bh, 0)) covers 4 queries,
-      // byte key mod 4 of each of its 4 words
-      uint32_t keep[4] = {0u, 0u, 0u, 0u};
+      // dropout: keep bits of this warpgroup's 64 query columns; one generator
+      // call (counter (query / 4, key / 4, bh, 0)) covers 4 queries, byte
+      // key mod 4 of each of its 4 words
+      uint32_t keep[2] = {0u, 0u};
       if constexpr (DROP) {
-        const uint32_t qb0 = 32u * (uint32_t)i;
+        const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
         const uint32_t sh = 8u * ((uint32_t)krow & 3u);
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        for (int m = 0; m < 16; ++m) {
           const uint4 w = philox4x32_10(qb0 + (uint32_t)m, (uint32_t)krow >> 2, (uint32_t)bh, 0u,
                                         p.drop.seed_lo, p.drop.seed_hi);
           const uint32_t bits = (((w.x >> sh) & 0xFFu) >= p.drop.t ? 1u : 0u) |
@@ -312,33 +314,34 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
       }
       auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
-      // the dV operand is the dropped P (P * Z * keep_scale)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      // the dV operand is the dropped P (P * Z * keep_scale), packed two
+      // queries per TMEM column into the first half of this warpgroup's own
+      // S columns (the other warpgroup may still be reading its half)
+      {
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const int c0 = 64 * hh + 2 * c;
+          const int c0 = 2 * c;
           if constexpr (DROP)
             pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
                                kept(c0 + 1) ? x[c0 + 1] * p.drop.keep_scale : 0.f);
           else
             pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
         }
-        tmem_st32(tS + lane_off + 32u * hh, pk);
+        tmem_st32(tS + lane_off + (uint32_t)cb, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(bar(L::bPFull));
 
-      // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> bf16 -> swizzled smem
+      // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> 16-bit -> swizzled smem
       if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)it & 1u, ctl, 122))) break;
       if (it > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(it - 1) & 1u, ctl, 123))) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t u[32];
-        tmem_ld32(tP + lane_off + 32u * cc, u);
+        tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, u);
         tmem_ld_wait(u);
         uint32_t pk[16];
 #pragma unroll
@@ -355,7 +358,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint8_t* dst = smem + L::kdS + swz_off(r, 32 * cc + 8 * k);
+          uint8_t* dst = smem + L::kdS + swz_off(r, cb + 32 * cc + 8 * k);
           *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
@@ -364,55 +367,51 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_arrive_warp(bar(L::bdSFull));
     }
 
-    // epilogue: dV and scale * dK for every key row of the tile (zeros when
-    // no query tile was live), staged in the K/V buffers and stored by TMA
+    // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK, for every key
+    // row of the tile (zeros when no query tile was live), staged in the V or
+    // K buffer and stored by TMA
     ok = __all_sync(0xFFFFFFFFu, ok);
     ok = ok && mbar_wait_warp(bar(L::bKV), 0, ctl, 124);
     const bool have = ok && len > 0 && mbar_wait_warp(bar(L::bFinal), 0, ctl, 125);
     tc_fence_after();
+    const uint32_t tacc = (cw == 0 ? tdV : tdK) + lane_off;
+    const float mul = (cw == 0) ? 1.f : scale;
+    uint8_t* stage = smem + (cw == 0 ? L::kV : L::kK);
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t tacc = (which == 0 ? tdV : tdK) + lane_off;
-      const float mul = (which == 0) ? 1.f : scale;
-      uint8_t* stage = smem + (which == 0 ? L::kV : L::kK);
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t u[32];
+      if (have) {
+        tmem_ld32(tacc + 32u * cc, u);
+        tmem_ld_wait(u);
+      } else {
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
-        if (have) {
-          tmem_ld32(tacc + 32u * cc, u);
-          tmem_ld_wait(u);
-        } else {
+        for (int c = 0; c < 32; ++c) u[c] = 0u;
+      }
+      uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) u[c] = 0u;
-        }
-        uint32_t pk[16];
+      for (int c = 0; c < 16; ++c)
+        pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
+    named_bar_sync(1 + cw, 128);
     if (r == 0) {
-      for (int h = 0; h < L::kHalves; ++h) {
-        tma_store_3d(&tdv, sbase + L::kV + h * 16384, 64 * h, kTile * kj, bh);
-        tma_store_3d(&tdk, sbase + L::kK + h * 16384, 64 * h, kTile * kj, bh);
-      }
+      for (int h = 0; h < L::kHalves; ++h)
+        tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + (cw == 0 ? L::kV : L::kK) + h * 16384, 64 * h, kTile * kj, bh);
       bulk_commit_group();
       bulk_wait_group_all();
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows in the dS buffer (two boxes of [128 rows x 32 fp32],
     // 128-byte swizzled) -> TMA reduce-add into the accumulator, 64 columns
-    // at a time; the dS buffer is handed back to warps 0-3 afterwards.
-    regs_inc<kDrainRegs>();
-    const int r = tid - 128;
+    // at a time; the dS buffer is handed back to warps 0-7 afterwards.
+    regs_dec<kDrainRegs>();
+    const int r = tid - 256;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     uint8_t* stage = smem + L::kdS;
     int i = next_live(0);
@@ -440,14 +439,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
               make_uint4(u1[4 * k], u1[4 * k + 1], u1[4 * k + 2], u1[4 * k + 3]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
+        named_bar_sync(3, 128);
         if (r == 0) {
           tma_reduce_add_3d(&tdq, smem_u32(stage), 64 * half, kTile * i, bh);
           tma_reduce_add_3d(&tdq, smem_u32(stage) + 16384u, 64 * half + 32, kTile * i, bh);
           bulk_commit_group();
           bulk_wait_group_read_all();      // staging may be rewritten
         }
-        named_bar_sync(2, 128);
+        named_bar_sync(3, 128);
       }
       if (r == 0) mbar_arrive(bar(L::bdSEmpty));
     }
@@ -456,7 +455,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
