@@ -19,14 +19,16 @@
 //        S^T  = K Q^T          (A = K, B = Q,   both K-major)
 //        dP^T = V dO^T         (A = V, B = dO,  both K-major)
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
-//        dK  += dS^T Q         (A = dS^T from smem K-major, B = Q MN-major)
+//        dK  += dS^T Q         (A = dS^T from TMEM, B = Q MN-major)
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
 //      S^T of the next query tile is issued after dK and dQ of the current one,
 //      which leaves its Q load the longest window.
-//      Each dQ partial is drained from TMEM into shared memory (the dS buffer,
-//      idle between the dQ MMA and the next dS) in two 64-column halves and
+//      Each dQ partial is drained from TMEM into shared memory (the dO ring
+//      slot of its own query tile, dead once dQ is issued, in two rounds) and
 //      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
-//      128-byte lines.
+//      128-byte lines. Q and the row statistics have their own barrier and are
+//      refilled as soon as dK has read Q; dO only after the reductions have
+//      read the slot.
 //      Warps: 0-3 and 4-7 recompute P and dS for query columns 0-63 and
 //      64-127 (thread = key row), 8-11 drain dQ from TMEM into the workspace
 //      (thread = query row), 12 TMA producer, 13 MMA, 14-15 idle (their
@@ -42,10 +44,10 @@ namespace fa {
 namespace {
 
 constexpr int kBwdThreads = 512;
-// per-thread registers after reallocation: 128 x (160 + 160 + 112 + 80) = 512 x 128
+// per-thread registers after reallocation: 128 x (160 + 160 + 96 + 96) = 512 x 128
 constexpr int kComputeRegs = 160;
-constexpr int kDrainRegs = 112;
-constexpr int kOtherRegs = 80;
+constexpr int kDrainRegs = 96;
+constexpr int kOtherRegs = 96;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
 
@@ -64,7 +66,9 @@ struct BwdLayout {
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kStages;
-  static constexpr int bSFull = bQEmpty + kStages;
+  static constexpr int bdOFull = bQEmpty + kStages;        // [stages]
+  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA
+  static constexpr int bSFull = bdOFree + kStages;
   static constexpr int bPFull = bSFull + 1;
   static constexpr int bdPFull = bPFull + 1;
   static constexpr int bdSFull = bdPFull + 1;
@@ -166,29 +170,39 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         tma_load_3d(sbase + L::kK + h * 16384, &tk, bar(L::bKV), 64 * h, kTile * kj, bh);
         tma_load_3d(sbase + L::kV + h * 16384, &tv, bar(L::bKV), 64 * h, kTile * kj, bh);
       }
-      int nq = 0;
+      int nq = 0, nd = 0;
       int i = next_live(0);
       for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
         const int s = it % L::kStages;
         const uint32_t n = (uint32_t)(it / L::kStages);
+        // Q and the row statistics once dK has read the slot's Q; dO once the
+        // dQ partial staged in the slot's dO buffer has been read
         if (it >= L::kStages && !mbar_wait(bar(L::bQEmpty + s), (n - 1) & 1u, ctl, 101)) break;
-        mbar_arrive_expect_tx(bar(L::bQFull + s), 2u * L::kTileBytes + 2u * kTile * 4u);
-        for (int h = 0; h < L::kHalves; ++h) {
+        mbar_arrive_expect_tx(bar(L::bQFull + s), L::kTileBytes + 2u * kTile * 4u);
+        for (int h = 0; h < L::kHalves; ++h)
           tma_load_3d(sbase + L::kQ + s * L::kTileBytes + h * 16384, &tq, bar(L::bQFull + s),
                       64 * h, kTile * i, bh);
-          tma_load_3d(sbase + L::kdO + s * L::kTileBytes + h * 16384, &tdo, bar(L::bQFull + s),
-                      64 * h, kTile * i, bh);
-        }
         const size_t roff = (size_t)bh * Np + (size_t)kTile * i;
         bulk_load(sbase + L::kRow + s * 1024, p.lse2 + roff, kTile * 4, bar(L::bQFull + s));
         bulk_load(sbase + L::kRow + s * 1024 + 512, p.delta + roff, kTile * 4, bar(L::bQFull + s));
         ++nq;
+        if (it >= L::kStages && !mbar_wait(bar(L::bdOFree + s), (n - 1) & 1u, ctl, 102)) break;
+        mbar_arrive_expect_tx(bar(L::bdOFull + s), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kdO + s * L::kTileBytes + h * 16384, &tdo, bar(L::bdOFull + s),
+                      64 * h, kTile * i, bh);
+        ++nd;
       }
       drain_wait(bar(L::bKV), 0);
       for (int s = 0; s < L::kStages; ++s)
+      {
         if (s < nq)
           drain_wait(bar(L::bQFull + s),
                      (uint32_t)((s + ((nq - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+        if (s < nd)
+          drain_wait(bar(L::bdOFull + s),
+                     (uint32_t)((s + ((nd - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -212,6 +226,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
         // dP^T = V dO^T (the dQ partial of the previous tile must have been read out)
         if (it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
+        if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 116))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
@@ -230,12 +245,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tdK, desc_kmajor(sdS, ks), desc_mnmajor(sQ, ks), idK, (it > 0 || ks > 0) ? 1u : 0u);
+          // dS^T of queries 0-63 in S columns 32-63, of queries 64-127 in 96-127
+          mma_ts(tdK, tS + 32u + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
+                 (it > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
           mma_ss(tP, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bdQFull));
-        mma_commit(bar(L::bQEmpty + s));
+        mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
         // next S^T (after this tile's dK and dQ: a longer window for its Q load)
         if (it + 1 < len) {
           const int s1 = (it + 1) % L::kStages;
@@ -288,7 +306,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
       // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
 #pragma unroll
-      for (int c = 0; c < 64; ++c) x[c] = ex2(fmaf(x[c], sl2, -lse2[c]));
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l = reinterpret_cast<const float4*>(lse2)[c4];   // one broadcast load per 4 queries
+        x[4 * c4] = ex2(fmaf(x[4 * c4], sl2, -l.x));
+        x[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], sl2, -l.y));
+        x[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], sl2, -l.z));
+        x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
+      }
       if (partial) {
         const int q0 = kTile * i + cb;
 #pragma unroll
@@ -352,16 +376,21 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             g0 = kept(c0) ? g0 * p.drop.keep_scale : 0.f;
             g1 = kept(c0 + 1) ? g1 * p.drop.keep_scale : 0.f;
           }
-          const float d0 = x[c0] * (g0 - dlt[c0]);
-          const float d1 = x[c0 + 1] * (g1 - dlt[c0 + 1]);
+          const float2 dl = reinterpret_cast<const float2*>(dlt)[c0 >> 1];
+          const float d0 = x[c0] * (g0 - dl.x);
+          const float d1 = x[c0 + 1] * (g1 - dl.y);
           pk[c] = pack2<F16>(d0, d1);
         }
+        // dS^T also goes to TMEM (the A operand of dK): the second half of this
+        // warpgroup's S columns, after its P
+        tmem_st16(tS + lane_off + 32u + (uint32_t)cb + 16u * cc, pk);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint8_t* dst = smem + L::kdS + swz_off(r, cb + 32 * cc + 8 * k);
           *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_warp(bar(L::bdSFull));
@@ -407,48 +436,66 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
-    // TMEM -> fp32 rows in the dS buffer (two boxes of [128 rows x 32 fp32],
-    // 128-byte swizzled) -> TMA reduce-add into the accumulator, 64 columns
-    // at a time; the dS buffer is handed back to warps 0-7 afterwards.
+    // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
+    // has completed) in two rounds of boxes of [128 rows x 32 fp32], 128-byte
+    // swizzled -> TMA reduce-add into the accumulator. The TMEM columns are
+    // released as soon as they are all in registers or staged; the slot goes
+    // back to the producer when the last round has been read.
     regs_dec<kDrainRegs>();
+    constexpr int kBoxesPerRound = L::kTileBytes / 16384;    // 1 (d = 64) or 2 (d = 128)
+    constexpr int kRounds = D / 32 / kBoxesPerRound;
     const int r = tid - 256;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    uint8_t* stage = smem + L::kdS;
+    const uint32_t sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
     int i = next_live(0);
     for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
-      // the dQ MMA (and the dK MMA before it) have completed: TMEM holds the
-      // partial and the dS buffer is no longer read by the tensor core
+      const int s = it % L::kStages;
+      const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
       if (!mbar_wait_warp(bar(L::bdQFull), (uint32_t)it & 1u, ctl, 130)) break;
       tc_fence_after();
+      uint32_t u[kBoxesPerRound][32];
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tP + lane_off + 64u * half, u0);
-        tmem_ld32(tP + lane_off + 64u * half + 32u, u1);
-        tmem_ld_wait(u0);
-        tmem_ld_wait(u1);
-        if (half == D / 64 - 1) {
+      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld32(tP + lane_off + 32u * b, u[b]);
+#pragma unroll
+      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
+#pragma unroll
+      for (int round = 0; round < kRounds; ++round) {
+        if (round == kRounds - 1) {
           tc_fence_before();
-          mbar_arrive_warp(bar(L::bdQFree));   // the TMEM columns may be overwritten
+          mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
+        }
+        if (round > 0) {              // the previous round has been read out of the slot
+          if (r == 0) bulk_wait_group_read_all();
+          named_bar_sync(3, 128);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {    // 8 chunks of 4 fp32 per 32-column box
-          const uint32_t sw = (uint32_t)(((k ^ (r & 7)) << 4) + (r >> 3) * 1024 + (r & 7) * 128);
-          *reinterpret_cast<uint4*>(stage + sw) = make_uint4(u0[4 * k], u0[4 * k + 1], u0[4 * k + 2], u0[4 * k + 3]);
-          *reinterpret_cast<uint4*>(stage + 16384 + sw) =
-              make_uint4(u1[4 * k], u1[4 * k + 1], u1[4 * k + 2], u1[4 * k + 3]);
-        }
+        for (int b = 0; b < kBoxesPerRound; ++b)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {    // 8 chunks of 4 fp32 per 32-column box
+            const uint32_t o = sw + (uint32_t)((k ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + stage + 16384 * b + o) =
+                make_uint4(u[b][4 * k], u[b][4 * k + 1], u[b][4 * k + 2], u[b][4 * k + 3]);
+          }
         fence_proxy_async_smem();
         named_bar_sync(3, 128);
         if (r == 0) {
-          tma_reduce_add_3d(&tdq, smem_u32(stage), 64 * half, kTile * i, bh);
-          tma_reduce_add_3d(&tdq, smem_u32(stage) + 16384u, 64 * half + 32, kTile * i, bh);
+#pragma unroll
+          for (int b = 0; b < kBoxesPerRound; ++b)
+            tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b), kTile * i, bh);
           bulk_commit_group();
-          bulk_wait_group_read_all();      // staging may be rewritten
         }
-        named_bar_sync(3, 128);
+        if (round + 1 < kRounds) {    // the next columns into registers while the round is read
+#pragma unroll
+          for (int b = 0; b < kBoxesPerRound; ++b)
+            tmem_ld32(tP + lane_off + 32u * ((round + 1) * kBoxesPerRound + b), u[b]);
+#pragma unroll
+          for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
+        }
       }
-      if (r == 0) mbar_arrive(bar(L::bdSEmpty));
+      if (r == 0) {
+        bulk_wait_group_read_all();
+        mbar_arrive(bar(L::bdOFree + s));
+      }
     }
     if (r == 0) bulk_wait_group_all();     // reductions complete before exit
   }
