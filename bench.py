@@ -15,7 +15,11 @@ ONE JSON line on stdout (rank 0):
   cpu_baseline the CPU float64 oracle on a bounded sample of the same workload
 
 `--impl reference` times the oracle itself (the CPU reference arm) on the
-same workload and metric. Several GPUs (torchrun) run independent replicas:
+same workload and metric. `--study io` and `--study memory` print one JSON
+line per measurement instead: the flash path against the standard
+(materialising) attention of include/standard_attn.h on one workload (time,
+FLOP, extra device memory; DRAM bytes come from an ncu capture of the same
+command), and the extra device memory of both over sequence lengths 128..64K. Several GPUs (torchrun) run independent replicas:
 the heads of different ranks never interact, so there is no collective on the
 data path, only a barrier and a max-reduction of the timings.
 """
@@ -43,7 +47,8 @@ def _args():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="long_causal")
+    ap.add_argument("--workload", default=None,
+                    help="workload name (default long_causal; gpt2m for --study io)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--p-drop", type=float, default=0.0,
@@ -52,6 +57,11 @@ def _args():
                     help="element type of Q, K, V, dO (and of the outputs)")
     ap.add_argument("--shape", default=None,
                     help="B,H,N override of the workload (smaller cases for profiler captures)")
+    ap.add_argument("--study", default=None, choices=["io", "memory"],
+                    help="flash vs standard attention: time/FLOP/memory on one workload (io), or "
+                         "extra device memory over N = 128..65536 (memory)")
+    ap.add_argument("--io-path", default="both", choices=["both", "flash", "standard"],
+                    help="--study io: which path to run (one path per ncu capture)")
     return ap.parse_args()
 
 
@@ -208,8 +218,7 @@ def run_reference(args):
     rank, world, _ = _dist_env()
     if rank != 0:
         return
-    from exact_io_aware_39_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = _resolve_workload(args, "long_causal")
     times, rates = [], []
     desc, cores = "", 1
     budget = max(0.5, 150.0 / max(1, args.steps + min(args.warmup, 1)))
@@ -229,6 +238,112 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _resolve_workload(args, default):
+    import dataclasses
+    from exact_io_aware_39_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload or default]
+    if args.shape:
+        sb, sh, sn = (int(x) for x in args.shape.split(","))
+        w = dataclasses.replace(w, B=sb, H=sh, N=sn, name=f"{w.name}@{sb}x{sh}x{sn}")
+    return w
+
+
+def _paths(fa, q, k, v, do, w, kv, bm):
+    """(name, fwd+bwd closure) of the flash and the standard path; each
+    closure allocates its own outputs and workspace, like a caller would."""
+    def flash():
+        o, lse = fa.attention_fwd(q, k, v, w.scale, w.causal, kv, bm)
+        return fa.attention_bwd(q, k, v, o, do, lse, w.scale, w.causal, kv, bm)
+
+    def standard():
+        o, lse, ws = fa.standard_attention_fwd(q, k, v, w.scale, w.causal, kv, bm)
+        return fa.standard_attention_bwd(q, k, v, do, ws, w.scale)
+    return {"flash": flash, "standard": standard}
+
+
+def run_study(args):
+    """Flash vs standard attention (no oracle involved): run time, FLOP and
+    extra device memory (everything a fwd+bwd call allocates beyond Q, K, V,
+    dO: outputs, LSE, workspaces)."""
+    import torch
+    import exact_io_aware_39_gb300 as fa
+    from exact_io_aware_39_gb300 import build as _build
+    from exact_io_aware_39_gb300.flops import attention_flops
+    from exact_io_aware_39_gb300.inputs import Workload, make_case
+    fa.load(_build.build())
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def measure(w, path_names, steps, warmup):
+        c = make_case(w)
+        B, H, N, d = c["B"], c["H"], c["N"], c["d"]
+        q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+        kv = None if c["kv_len"] is None else c["kv_len"].to(dev)
+        bm = None if c["block_mask"] is None else c["block_mask"].to(dev)
+        kv_np = None if c["kv_len"] is None else c["kv_len"].numpy()
+        bm_np = None if c["block_mask"] is None else c["block_mask"].numpy()
+        f_fwd, f_bwd = attention_flops(B, H, N, d, w.causal, kv_np, bm_np)
+        dense = 4.0 * d * N * N * B * H
+        runs = _paths(fa, q, k, v, do, w, kv, bm)
+        out = []
+        for name in path_names:
+            run = runs[name]
+            torch.cuda.synchronize()
+            base = torch.cuda.memory_allocated(dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            res = run()
+            torch.cuda.synchronize()
+            extra = torch.cuda.max_memory_allocated(dev) - base
+            del res
+            for _ in range(warmup):
+                run()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / max(1, steps)
+            st, detail = fa.device_error()
+            if st != 0:
+                raise RuntimeError(f"device error: {detail}")
+            flop = (f_fwd + f_bwd) if name == "flash" else 3.0 * dense   # standard: 6 dense GEMMs
+            out.append({"path": name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                        "ms_fwd_bwd": ms, "gflop": flop / 1e9, "tflops": flop / (ms * 1e-3) / 1e12,
+                        "extra_device_bytes": extra, "iterations_run": 1 + warmup + steps})
+        return out
+
+    if args.study == "io":
+        w = _resolve_workload(args, "gpt2m")
+        names = ["flash", "standard"] if args.io_path == "both" else [args.io_path]
+        for rec in measure(w, names, args.steps, args.warmup):
+            rec.update({"study": "io", "workload": w.name,
+                        "note": "standard = cuBLAS GEMMs with S and P in device memory (S, dP fp32; "
+                                "P, dS 16-bit); its FLOP are dense (masks do not remove work)"})
+            print(json.dumps(rec), flush=True)
+    else:
+        cap = 64 << 30          # standard path only while its workspace stays below 64 GiB
+        Bm, Hm = 1, 16
+        if args.shape:
+            Bm, Hm = (int(x) for x in args.shape.split(",")[:2])
+        N = 128
+        while N <= 65536:
+            w = Workload(f"sweep_N{N}", Bm, Hm, N, 64, False, 0.125)
+            names = ["flash"]
+            if fa.standard_attn_workspace_size(Bm, Hm, N) <= cap:
+                names.append("standard")
+            for rec in measure(w, names, 1, 1):
+                rec.update({"study": "memory"})
+                print(json.dumps(rec), flush=True)
+            if "standard" not in names:
+                ws = fa.standard_attn_workspace_size(Bm, Hm, N)
+                print(json.dumps({"study": "memory", "path": "standard", "B": Bm, "H": Hm, "N": N, "d": 64,
+                                  "not_run": f"workspace {ws} bytes above the {cap} byte cap",
+                                  "extra_device_bytes_lower_bound": ws}), flush=True)
+            N *= 2
+
+
 def run_ours(args):
     import torch
     rank, world, local = _dist_env()
@@ -242,15 +357,11 @@ def run_ours(args):
     import exact_io_aware_39_gb300 as fa
     from exact_io_aware_39_gb300 import build as _build
     from exact_io_aware_39_gb300.flops import attention_flops
-    from exact_io_aware_39_gb300.inputs import WORKLOADS, make_case
+    from exact_io_aware_39_gb300.inputs import make_case
     from exact_io_aware_39_gb300.replicas import job_throughput, max_over_ranks
     fa.load(_build.build() if rank == 0 or world == 1 else _build.LIB_PATH)
 
-    w = WORKLOADS[args.workload]
-    if args.shape:
-        import dataclasses
-        sb, sh, sn = (int(x) for x in args.shape.split(","))
-        w = dataclasses.replace(w, B=sb, H=sh, N=sn, name=f"{w.name}@{sb}x{sh}x{sn}")
+    w = _resolve_workload(args, "long_causal")
     c = make_case(w, dtype=torch.float16 if args.dtype == "f16" else torch.bfloat16)
     B, H, N, d = c["B"], c["H"], c["N"], c["d"]
     kv_np = None if c["kv_len"] is None else c["kv_len"].numpy()
@@ -434,7 +545,9 @@ def run_ours(args):
 
 def main():
     args = _args()
-    if args.impl == "reference":
+    if args.study:
+        run_study(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

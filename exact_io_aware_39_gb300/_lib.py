@@ -22,13 +22,14 @@ STATUS_NAMES = {
 FA_ERR_SCRATCH_LIMIT = 7
 BWD_NOALLOC_SCRATCH_BYTES = 64 << 20
 
-# every symbol include/flash_attn.h declares
+# every symbol include/flash_attn.h and include/standard_attn.h declare
 EXPORTS = [
     "flash_attn_fwd", "flash_attn_fwd_ex", "flash_attn_bwd_workspace_size", "flash_attn_bwd",
     "flash_attn_bwd_ex", "flash_attn_bwd_noalloc",
     "flash_attn_tile_map",
     "flash_attn_get_device_error", "flash_attn_set_profile_events", "flash_attn_status_string",
     "flash_attn_version",
+    "standard_attn_workspace_size", "standard_attn_fwd", "standard_attn_bwd",
 ]
 
 
@@ -85,6 +86,12 @@ def load(path=LIB_PATH):
     lib.flash_attn_status_string.restype = ctypes.c_char_p
     lib.flash_attn_version.argtypes = []
     lib.flash_attn_version.restype = i32
+    lib.standard_attn_workspace_size.argtypes = [i32, i32, i32]
+    lib.standard_attn_workspace_size.restype = sz
+    lib.standard_attn_fwd.argtypes = [vp] * 5 + [i32, i32, i32, i32, f32, i32, vp, vp, opt_p, vp, sz, vp]
+    lib.standard_attn_fwd.restype = i32
+    lib.standard_attn_bwd.argtypes = [vp] * 7 + [i32, i32, i32, i32, f32, opt_p, vp, sz, vp]
+    lib.standard_attn_bwd.restype = i32
     _lib = lib
     return lib
 
@@ -147,6 +154,23 @@ def flash_attn_status_string(status):
 
 def flash_attn_version():
     return load().flash_attn_version()
+
+
+def standard_attn_workspace_size(B, H, N):
+    return load().standard_attn_workspace_size(B, H, N)
+
+
+def standard_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, options, workspace,
+                      workspace_bytes, stream):
+    return load().standard_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask,
+                                    None if options is None else ctypes.byref(options), workspace,
+                                    workspace_bytes, stream)
+
+
+def standard_attn_bwd(Q, K, V, dO, dQ, dK, dV, B, H, N, d, scale, options, workspace, workspace_bytes, stream):
+    return load().standard_attn_bwd(Q, K, V, dO, dQ, dK, dV, B, H, N, d, scale,
+                                    None if options is None else ctypes.byref(options), workspace,
+                                    workspace_bytes, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -255,3 +279,38 @@ def profile_next_call(start, stop):
 def device_error():
     """(status, [code, site, block, thread]) of the device error word; clears it."""
     return flash_attn_get_device_error()
+
+
+def standard_attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, workspace=None,
+                           stream=None):
+    """Standard (materialising) attention on the GPU: (O, LSE, workspace); the
+    workspace holds S and P and must be passed to standard_attention_bwd."""
+    import torch
+    opts = _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = standard_attn_workspace_size(B, H, N)
+    if need == 0:
+        raise FlashAttnError(2, "standard_attn_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    kv_p, bm_p = _mask_args(kv_len, block_mask)
+    st = standard_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, float(scale),
+                           int(bool(causal)), kv_p, bm_p, opts, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "standard_attn_fwd")
+    return o, l, workspace
+
+
+def standard_attention_bwd(q, k, v, do, workspace, scale, stream=None):
+    """dQ, dK, dV of standard attention from the P the forward call stored."""
+    import torch
+    opts = _check_inputs(q, k, v, do)
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = standard_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                           float(scale), opts, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _check(st, "standard_attn_bwd")
+    return dq, dk, dv

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libflashattn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "std_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I", INCLUDE, "-I", CSRC]
@@ -34,6 +34,17 @@ def nvcc():
     if exe is None:
         raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the library")
     return exe
+
+
+def link_flags():
+    """cuBLAS (the plain GEMMs of the standard-attention baseline), found next
+    to the nvcc in use and recorded as the library's run path."""
+    cuda_home = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
+    dirs = [d for d in (os.path.join(cuda_home, "lib64"), os.path.join(cuda_home, "lib")) if os.path.isdir(d)]
+    flags = ["-lcublas"]
+    for d in dirs:
+        flags += ["-L", d, "-Xlinker", "-rpath=" + d]
+    return flags
 
 
 def _stale(obj, deps):
@@ -70,7 +81,7 @@ def build(verbose=False, extra_flags=()):
         raise RuntimeError(f"nvcc failed:\n{msg}")
     if procs or not os.path.exists(LIB_PATH) or _stale(LIB_PATH, objs):
         tmp = LIB_PATH + ".tmp"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, *link_flags()]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)

@@ -173,6 +173,16 @@ int internal_device_error_word(unsigned int** err) {
   return st;
 }
 
+int internal_read_options(const void* options, bool* f16, bool* dropout) {
+  Options o;
+  const fa_status st = read_options(static_cast<const fa_options*>(options), &o);
+  if (st == FA_OK) {
+    *f16 = o.f16;
+    *dropout = o.drop.t != 0u;
+  }
+  return st;
+}
+
 int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return make_map(m, base, BH, N, d);
 }

@@ -102,6 +102,7 @@ cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_
 // Host helpers defined with the C ABI (return fa_status values).
 int internal_check_shape(int B, int H, int N, int d, float scale, int causal);
 int internal_device_error_word(unsigned int** err);   // current device; runs its set-up once
+int internal_read_options(const void* options, bool* f16, bool* dropout);   // options: const fa_options*
 int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d);   // bf16
 int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, int d);
 

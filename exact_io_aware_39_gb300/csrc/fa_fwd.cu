@@ -79,9 +79,6 @@ struct FwdLayout {
 __device__ __forceinline__ int entry_j(uint32_t e) { return (int)(e & 0x3FFu); }
 __device__ __forceinline__ uint32_t entry_live(uint32_t e, int t) { return (e >> (10 + t)) & 1u; }
 __device__ __forceinline__ uint32_t entry_partial(uint32_t e, int t) { return (e >> (12 + t)) & 1u; }
-__device__ __forceinline__ uint32_t entry_nlive(uint32_t e) {
-  return entry_live(e, 0) + entry_live(e, 1);
-}
 
 template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kFwdThreads, 1)

@@ -20,9 +20,13 @@ def lib():
 
 
 def _declared():
-    txt = open(os.path.join(ROOT, "include", "flash_attn.h")).read()
-    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(flash_attn_\w+)\s*\(", txt)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b((?:flash|standard)_attn_\w+)\s*\(", txt))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -92,3 +96,30 @@ def test_options_validated_before_any_launch(lib):
     ws = L.flash_attn_bwd_workspace_size(1, 1, 128, 64)
     args = [p] * 9 + [1, 1, 128, 64, 0.1, 0, None, None]
     assert L.flash_attn_bwd_ex(*args, bad_dtype, p, ws, None) == 2
+
+
+def test_standard_workspace_size_formula(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    def al(x):
+        return (x + 255) // 256 * 256
+    for B, H, N in [(1, 2, 256), (2, 3, 300), (8, 16, 1024)]:
+        nn = B * H * N * N
+        assert L.standard_attn_workspace_size(B, H, N) == al(nn * 4) + al(nn * 2)
+    assert L.standard_attn_workspace_size(0, 1, 128) == 0
+    assert L.standard_attn_workspace_size(1, 1, 65537) == 0
+
+
+def test_standard_attn_arguments_validated_before_any_launch(lib):
+    from exact_io_aware_39_gb300 import _lib as L
+    p = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    ws = L.standard_attn_workspace_size(1, 1, 128)
+    def fwd(*, d=64, N=128, causal=0, opts=None, w=p, nbytes=ws, q=p, scale=0.1):
+        return L.standard_attn_fwd(q, p, p, p, p, 1, 1, N, d, scale, causal, None, None, opts, w, nbytes, None)
+    assert fwd(q=None) == 1 and fwd(q=bad) == 1 and fwd(causal=2) == 1 and fwd(scale=float("nan")) == 1
+    assert fwd(d=60) == 2 and fwd(d=264) == 2 and fwd(N=65537) == 2
+    assert fwd(opts=L.fa_options(p_drop=0.1)) == 2        # dropout is not part of the baseline
+    assert fwd(opts=L.fa_options(7)) == 2
+    assert fwd(nbytes=ws - 1) == 3 and fwd(w=None) == 3 and fwd(w=ctypes.c_void_p((1 << 20) + 16)) == 3
+    assert L.standard_attn_bwd(p, p, p, p, p, p, None, 1, 1, 128, 64, 0.1, None, p, ws, None) == 1
+    assert L.standard_attn_bwd(p, p, p, p, p, p, p, 1, 1, 128, 64, 0.1, None, p, ws - 1, None) == 3
