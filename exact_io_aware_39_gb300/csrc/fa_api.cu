@@ -140,7 +140,7 @@ fa_status read_options(const fa_options* opt, Options* out) {
 fa_status check_shape(int B, int H, int N, int d, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1 || !std::isfinite(scale) || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d < 8 || d > 128 || (d % 8) != 0) return FA_ERR_UNSUPPORTED;
   if (N > kMaxN) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
   const long long nT = (N + kTile - 1) / kTile;
@@ -297,6 +297,7 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.drop = o.drop;
+  p.d = d;
   const ProfileScope prof(s);
   prof.before();
   const cudaError_t e = launch_bwd_main(d, o.f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);

@@ -481,7 +481,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (r == 0) {
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b)
-            tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b), kTile * i, bh);
+            if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
+              tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b), kTile * i, bh);
           bulk_commit_group();
         }
         if (round + 1 < kRounds) {    // the next columns into registers while the round is read
@@ -509,22 +510,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 }
 
 // D = rowsum(dO * O) (fp32), LSE2 = LSE * log2(e) with +inf for -inf and
-// padding rows, dQ accumulator zeroed. One group of d/8 threads per row, each
-// owning 8 consecutive columns.
-template <int D, bool F16>
+// padding rows, dQ accumulator zeroed. A group of G threads per row (G the
+// power of two >= d / 8); thread `part` owns columns 8 part .. 8 part + 7 when
+// 8 part < d.
+template <int G, bool F16>
 __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                   const float* __restrict__ lse, float* __restrict__ dq_acc,
-                                  float* __restrict__ lse2, float* __restrict__ delta, int BH, int N, int Np) {
-  constexpr int G = D / 8;   // threads per row
+                                  float* __restrict__ lse2, float* __restrict__ delta, int BH, int N, int Np,
+                                  int d) {
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gid / G;           // over BH * Np
   const int part = (int)(gid % G);
-  if (row >= (long long)BH * Np) return;
+  if (row >= (long long)BH * Np) return;   // whole groups leave together (G divides the block)
   const int bh = (int)(row / Np);
   const int n = (int)(row % Np);
+  const bool mine = 8 * part < d;
   float acc = 0.f;
-  if (n < N) {
-    const size_t off = ((size_t)bh * N + n) * D + part * 8;
+  if (n < N && mine) {
+    const size_t off = ((size_t)bh * N + n) * d + part * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(o + off);
     const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
@@ -538,9 +541,11 @@ __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t
   }
 #pragma unroll
   for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D + part * 8);
-  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mine) {
+    float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * d + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (part == 0) {
     delta[row] = acc;
     float v = INFINITY;
@@ -552,24 +557,26 @@ __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t
   }
 }
 
-template <int D, bool F16>
+// dQ = 16-bit(scale * dQ accumulator), one thread per 8 columns.
+template <bool F16>
 __global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, float scale,
-                                 int BH, int N, int Np) {
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // one thread per 8 columns
-  const long long total = (long long)BH * N * (D / 8);
+                                 int BH, int N, int Np, int d) {
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int parts = d / 8;
+  const long long total = (long long)BH * N * parts;
   if (gid >= total) return;
-  const long long row = gid / (D / 8);
-  const int part = (int)(gid % (D / 8));
+  const long long row = gid / parts;
+  const int part = (int)(gid % parts);
   const int bh = (int)(row / N);
   const int n = (int)(row % N);
-  const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Np + n) * D + part * 8);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Np + n) * d + part * 8);
   const float4 a = src[0], c = src[1];
   uint4 out;
   out.x = pack2<F16>(a.x * scale, a.y * scale);
   out.y = pack2<F16>(a.z * scale, a.w * scale);
   out.z = pack2<F16>(c.x * scale, c.y * scale);
   out.w = pack2<F16>(c.z * scale, c.w * scale);
-  *reinterpret_cast<uint4*>(dq + (size_t)row * D + part * 8) = out;
+  *reinterpret_cast<uint4*>(dq + (size_t)row * d + part * 8) = out;
 }
 
 template <int D, bool F16, bool DROP>
@@ -589,37 +596,33 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   return cudaGetLastError();
 }
 
-template <int D, bool F16>
-void launch_bwd_pre_d(const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
-                      float* delta, int BH, int N, int Np, cudaStream_t s) {
-  const long long threads = (long long)BH * Np * (D / 8);
-  const int block = 256;
-  const unsigned grid = (unsigned)((threads + block - 1) / block);
-  fa_bwd_pre_kernel<D, F16><<<grid, block, 0, s>>>(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                                   lse, dq_acc, lse2, delta, BH, N, Np);
-}
-
-template <int D, bool F16>
-void launch_bwd_dq_d(const float* dq_acc, void* dq, float scale, int BH, int N, int Np, cudaStream_t s) {
-  const long long threads = (long long)BH * N * (D / 8);
-  const int block = 256;
-  const unsigned grid = (unsigned)((threads + block - 1) / block);
-  fa_bwd_dq_kernel<D, F16><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np);
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
                            float* delta, int BH, int N, int nT, int d, cudaStream_t s) {
   const int Np = nT * kTile;
-  if (f16) {
-    if (d == 64) launch_bwd_pre_d<64, true>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
-    else launch_bwd_pre_d<128, true>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
-  } else {
-    if (d == 64) launch_bwd_pre_d<64, false>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
-    else launch_bwd_pre_d<128, false>(o, dout, lse, dq_acc, lse2, delta, BH, N, Np, s);
+  int G = 1;
+  while (G < d / 8) G <<= 1;              // 1 .. 16: divides the block and the warp
+  const long long threads = (long long)BH * Np * G;
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  const uint16_t* o16 = static_cast<const uint16_t*>(o);
+  const uint16_t* g16 = static_cast<const uint16_t*>(dout);
+#define FA_PRE_CASE(GG)                                                                                     \
+  if (G == GG) {                                                                                            \
+    if (f16)                                                                                                \
+      fa_bwd_pre_kernel<GG, true><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, BH, N, Np, d);  \
+    else                                                                                                    \
+      fa_bwd_pre_kernel<GG, false><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, BH, N, Np, d); \
+    return cudaGetLastError();                                                                              \
   }
-  return cudaGetLastError();
+  FA_PRE_CASE(1)
+  FA_PRE_CASE(2)
+  FA_PRE_CASE(4)
+  FA_PRE_CASE(8)
+  FA_PRE_CASE(16)
+#undef FA_PRE_CASE
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -627,8 +630,9 @@ cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtens
                             const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s) {
   const float scale = p.scale_log2 / 1.4426950408889634f;
   const bool drop = p.drop.t > 0;
+  const int kd = kernel_head_dim(d);
 #define FA_BWD_CASE(DD, FF, DR) \
-  if (d == DD && f16 == FF && drop == DR) \
+  if (kd == DD && f16 == FF && drop == DR) \
     return launch_bwd_main_d<DD, FF, DR>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);
   FA_BWD_CASE(64, false, false)
   FA_BWD_CASE(128, false, false)
@@ -646,13 +650,13 @@ cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, 
                           cudaStream_t s) {
   const int Np = nT * kTile;
   if ((long long)BH * N == 0) return cudaSuccess;
-  if (f16) {
-    if (d == 64) launch_bwd_dq_d<64, true>(dq_acc, dq, scale, BH, N, Np, s);
-    else launch_bwd_dq_d<128, true>(dq_acc, dq, scale, BH, N, Np, s);
-  } else {
-    if (d == 64) launch_bwd_dq_d<64, false>(dq_acc, dq, scale, BH, N, Np, s);
-    else launch_bwd_dq_d<128, false>(dq_acc, dq, scale, BH, N, Np, s);
-  }
+  const long long threads = (long long)BH * N * (d / 8);
+  const int block = 256;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
+  if (f16)
+    fa_bwd_dq_kernel<true><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
+  else
+    fa_bwd_dq_kernel<false><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
   return cudaGetLastError();
 }
 

@@ -72,10 +72,17 @@ struct BwdParams {
   int causal;
   float scale_log2;
   DropoutParams drop;
+  int d;                      // head dimension of the tensors (<= the kernel's tile width)
 };
 
+// Head dimension of the kernel that serves a head dimension d (a multiple of
+// 8 up to 128): tiles are 64 or 128 columns wide; columns past d are zeros on
+// load (TMA out-of-bounds fill) and are not written on store.
+__host__ __device__ __forceinline__ int kernel_head_dim(int d) { return d <= 64 ? 64 : 128; }
+
 // Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1,
-// 128-byte swizzle. Return the cudaError_t of the launch.
+// 128-byte swizzle. d is the tensors' head dimension; the kernel instance is
+// chosen by kernel_head_dim(d). Return the cudaError_t of the launch.
 // f16 selects fp16 elements (else bf16) for Q, K, V, O, dO, dQ, dK, dV.
 // dropout is applied when p.drop.t > 0.
 cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

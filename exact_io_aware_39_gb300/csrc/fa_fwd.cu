@@ -479,8 +479,9 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   const bool drop = p.drop.t > 0;
+  const int kd = kernel_head_dim(d);
 #define FA_FWD_CASE(DD, FF, DR) \
-  if (d == DD && f16 == FF && drop == DR) return launch_fwd_d<DD, FF, DR>(tq, tk, tv, to, p, s);
+  if (kd == DD && f16 == FF && drop == DR) return launch_fwd_d<DD, FF, DR>(tq, tk, tv, to, p, s);
   FA_FWD_CASE(64, false, false)
   FA_FWD_CASE(128, false, false)
   FA_FWD_CASE(64, true, false)

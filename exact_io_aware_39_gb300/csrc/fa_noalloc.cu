@@ -107,6 +107,7 @@ extern "C" fa_status flash_attn_bwd_noalloc(const void* Q, const void* K, const 
   p.nT = nT;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.d = d;
   if (launch_bwd_main(d, false, tq, tk, tv, tdo, tdk, tdv, tdq, p, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_dq(false, dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;

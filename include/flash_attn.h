@@ -15,7 +15,11 @@
  *      Q, K, V, O, dO, dQ, dK, dV : bfloat16 [B, H, N, d] (fp16 through the
  *                                   *_ex calls)
  *      LSE                         : float32  [B, H, N]
- *    N is the sequence length of both queries and keys. d is 64 or 128.
+ *    N is the sequence length of both queries and keys. d is a multiple of
+ *    8 from 8 to 128: 64 and 128 run on kernels of exactly that width; any
+ *    other d runs on the 64- (d < 64) or 128-column (d > 64) kernel over
+ *    tiles whose columns past d are zero (the arithmetic of the padded
+ *    width is spent, the result is that of width d).
  *  - Every pointer named here is a DEVICE pointer of the current CUDA device,
  *    16-byte aligned, owned by the caller (the library keeps no reference
  *    after the call returns and allocates no device memory).
@@ -49,7 +53,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size, non-finite scale */
-  FA_ERR_UNSUPPORTED = 2,      /* d not in {64, 128}, N > 131072, no sm_103a device */
+  FA_ERR_UNSUPPORTED = 2,      /* d not a multiple of 8 in [8, 128], N > 131072, no sm_103a device */
   FA_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small */
   FA_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
   FA_ERR_DEVICE_TIMEOUT = 5,   /* a kernel's bounded wait ran out (device error word) */
@@ -98,7 +102,7 @@ typedef struct {
  *   Q, K, V : in,  bf16 [B, H, N, d]
  *   O       : out, bf16 [B, H, N, d]
  *   LSE     : out, fp32 [B, H, N]
- *   B, H >= 1; 1 <= N <= 131072; d in {64, 128}; scale finite;
+ *   B, H >= 1; 1 <= N <= 131072; d a multiple of 8 in [8, 128]; scale finite;
  *   causal 0 or 1; kv_len, block_mask as above (may be NULL).
  */
 fa_status flash_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,

@@ -4,9 +4,10 @@ oracle's dropout, and bit-exact keep masks from both kernels' generators.
 Tolerances as for the other parity tests (LSE max-abs <= 1e-3, dQ/dK/dV
 relative Frobenius <= 2e-2), except O: dropout multiplies the kept values by
 s = 256 / (256 - t), so O can reach s times the magnitudes of the undropped
-case and its bf16 rounding error grows by the same factor (at p = 0.5, early
-causal rows reach |O| ~ 9, where half a bf16 ulp is 0.016). The O bound is
-therefore 1e-2 * s. The keep masks are compared bit for bit.
+case, and rounding O to bf16 (8 significant bits) alone moves an element by
+up to 2^-8 |O| (0.016 at |O| = 4.1, 0.035 at |O| = 9 in early causal rows at
+p = 0.5). The O bound is therefore elementwise 1e-2 * s + 2^-8 |O_ref|. The
+keep masks are compared bit for bit.
 """
 import math
 import zlib
@@ -41,6 +42,7 @@ CASES = [
     ("d64_kv_len", 3, 2, 300, 64, False, [300, 5, 130], False, 0.25, 2**40 + 3, torch.bfloat16),
     ("d128_block_mask", 1, 2, 640, 128, True, None, True, 0.2, 5, torch.bfloat16),
     ("fp16_d128", 1, 2, 384, 128, False, None, False, 0.3, 42, torch.float16),
+    ("d80_causal", 1, 2, 300, 80, True, None, False, 0.2, 77, torch.bfloat16),
 ]
 
 
@@ -72,8 +74,9 @@ def test_dropout_matches_oracle(fa, spec):
     assert fa.device_error()[0] == 0
     ref = oracle.attention_fwd_bwd_dropout(c["q"], c["k"], c["v"], c["do"], c["scale"], c["causal"],
                                            c["kv_len"], c["block_mask"], p_drop=p, seed=seed)
-    o_err = np.abs(o.float().cpu().numpy() - ref["O"]).max()
-    assert o_err <= O_TOL * oracle.threshold(p)[1], o_err
+    o_abs = np.abs(o.float().cpu().numpy() - ref["O"])
+    bound = O_TOL * oracle.threshold(p)[1] + 2.0 ** -8 * np.abs(ref["O"])
+    assert (o_abs <= bound).all(), (o_abs.max(), (o_abs - bound).max())
     lr, lg = ref["LSE"], lse.cpu().numpy()
     fin = np.isfinite(lr)
     assert np.array_equal(fin, np.isfinite(lg))
