@@ -88,9 +88,9 @@ def load(path=LIB_PATH):
     lib.flash_attn_version.restype = i32
     lib.standard_attn_workspace_size.argtypes = [i32, i32, i32]
     lib.standard_attn_workspace_size.restype = sz
-    lib.standard_attn_fwd.argtypes = [vp] * 5 + [i32, i32, i32, i32, f32, i32, vp, vp, opt_p, vp, sz, vp]
+    lib.standard_attn_fwd.argtypes = [vp] * 5 + [i32, i32, i32, i32, f32, i32, vp, vp, opt_p, i32, vp, sz, vp]
     lib.standard_attn_fwd.restype = i32
-    lib.standard_attn_bwd.argtypes = [vp] * 7 + [i32, i32, i32, i32, f32, opt_p, vp, sz, vp]
+    lib.standard_attn_bwd.argtypes = [vp] * 7 + [i32, i32, i32, i32, f32, opt_p, i32, vp, sz, vp]
     lib.standard_attn_bwd.restype = i32
     _lib = lib
     return lib
@@ -160,16 +160,20 @@ def standard_attn_workspace_size(B, H, N):
     return load().standard_attn_workspace_size(B, H, N)
 
 
-def standard_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, options, workspace,
+STANDARD_ATTN_S16 = 1
+
+
+def standard_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask, options, flags, workspace,
                       workspace_bytes, stream):
     return load().standard_attn_fwd(Q, K, V, O, LSE, B, H, N, d, scale, causal, kv_len, block_mask,
-                                    None if options is None else ctypes.byref(options), workspace,
+                                    None if options is None else ctypes.byref(options), flags, workspace,
                                     workspace_bytes, stream)
 
 
-def standard_attn_bwd(Q, K, V, dO, dQ, dK, dV, B, H, N, d, scale, options, workspace, workspace_bytes, stream):
+def standard_attn_bwd(Q, K, V, dO, dQ, dK, dV, B, H, N, d, scale, options, flags, workspace, workspace_bytes,
+                      stream):
     return load().standard_attn_bwd(Q, K, V, dO, dQ, dK, dV, B, H, N, d, scale,
-                                    None if options is None else ctypes.byref(options), workspace,
+                                    None if options is None else ctypes.byref(options), flags, workspace,
                                     workspace_bytes, stream)
 
 
@@ -282,9 +286,10 @@ def device_error():
 
 
 def standard_attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, workspace=None,
-                           stream=None):
+                           stream=None, s16=False):
     """Standard (materialising) attention on the GPU: (O, LSE, workspace); the
-    workspace holds S and P and must be passed to standard_attention_bwd."""
+    workspace holds S and P and must be passed to standard_attention_bwd.
+    s16=True stores S (and later dP) in the 16-bit input type."""
     import torch
     opts = _check_inputs(q, k, v)
     B, H, N, d = q.shape
@@ -297,20 +302,22 @@ def standard_attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     kv_p, bm_p = _mask_args(kv_len, block_mask)
     st = standard_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l), B, H, N, d, float(scale),
-                           int(bool(causal)), kv_p, bm_p, opts, _ptr(workspace),
+                           int(bool(causal)), kv_p, bm_p, opts, STANDARD_ATTN_S16 if s16 else 0, _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "standard_attn_fwd")
     return o, l, workspace
 
 
-def standard_attention_bwd(q, k, v, do, workspace, scale, stream=None):
-    """dQ, dK, dV of standard attention from the P the forward call stored."""
+def standard_attention_bwd(q, k, v, do, workspace, scale, stream=None, s16=False):
+    """dQ, dK, dV of standard attention from the P the forward call stored
+    (s16 as in the forward call)."""
     import torch
     opts = _check_inputs(q, k, v, do)
     B, H, N, d = q.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     st = standard_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
-                           float(scale), opts, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           float(scale), opts, STANDARD_ATTN_S16 if s16 else 0, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(),
                            _stream(stream))
     _check(st, "standard_attn_bwd")
     return dq, dk, dv

@@ -34,6 +34,25 @@ __device__ __forceinline__ uint16_t to16(float x) {
 
 constexpr int kRowsPerCta = kRowThreads / 32;   // one warp per row
 
+// Element e (and e .. e + 3, 16-byte / 8-byte aligned for rows with N a
+// multiple of 4) of a stored score-like matrix: fp32, or the 16-bit input type.
+template <bool F16, bool S16>
+__device__ __forceinline__ float4 row_load4(const void* base, size_t e) {
+  if constexpr (S16) {
+    const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e);
+    return make_float4(load16<F16>(v.x & 0xFFFFu), load16<F16>(v.x >> 16), load16<F16>(v.y & 0xFFFFu),
+                       load16<F16>(v.y >> 16));
+  } else {
+    return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + e);
+  }
+}
+
+template <bool F16, bool S16>
+__device__ __forceinline__ float row_load1(const void* base, size_t e) {
+  if constexpr (S16) return load16<F16>(static_cast<const uint16_t*>(base)[e]);
+  else return static_cast<const float*>(base)[e];
+}
+
 // Warp-wide combination of per-lane (max, sum of exp(x - max)) pairs.
 __device__ __forceinline__ void warp_max_sum(float& m, float& l) {
 #pragma unroll
@@ -65,8 +84,8 @@ __device__ __forceinline__ void online_add(float x, float& m, float& l) {
 // scaled) scores. P_ij = exp(S_ij - LSE_i) on allowed keys, 0 elsewhere;
 // LSE_i = max + ln(sum exp(S_ij - max)), -inf for a row with no allowed key.
 // Rows with N a multiple of 4 are read as float4 (16-byte aligned rows).
-template <bool F16>
-__global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const float* __restrict__ S,
+template <bool F16, bool S16>
+__global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const void* __restrict__ Sv,
                                                                   uint16_t* __restrict__ P, float* __restrict__ lse,
                                                                   long long rows, int H, int N, int nT, int causal,
                                                                   const int32_t* kv_len, const uint8_t* bm) {
@@ -77,7 +96,6 @@ __global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const float* _
   const int b = (int)(row / N) / H;
   const int kvl = effective_kv_len(kv_len, b, N);
   const int jmax = causal ? min(kvl, i + 1) : kvl;          // allowed keys are j < jmax ...
-  const float* s = S + (size_t)row * N;
   uint16_t* p = P + (size_t)row * N;
   const uint8_t* bmrow = bm ? bm + (size_t)(i / kTile) * nT : nullptr;
   auto allowed = [&](int j) -> bool {                        // ... and not in a masked block
@@ -85,9 +103,11 @@ __global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const float* _
   };
   float m = -INFINITY, l = 0.f;
   const bool vec = (N & 3) == 0;
+  auto load4 = [&](int j) -> float4 { return row_load4<F16, S16>(Sv, (size_t)row * N + j); };
+  auto load1 = [&](int j) -> float { return row_load1<F16, S16>(Sv, (size_t)row * N + j); };
   if (vec) {
     for (int j = 4 * lane; j < N; j += 128) {
-      const float4 x = *reinterpret_cast<const float4*>(s + j);
+      const float4 x = load4(j);
       if (allowed(j)) online_add(x.x, m, l);
       if (allowed(j + 1)) online_add(x.y, m, l);
       if (allowed(j + 2)) online_add(x.z, m, l);
@@ -95,13 +115,13 @@ __global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const float* _
     }
   } else {
     for (int j = lane; j < N; j += 32)
-      if (allowed(j)) online_add(s[j], m, l);
+      if (allowed(j)) online_add(load1(j), m, l);
   }
   warp_max_sum(m, l);
   const float L = (m == -INFINITY) ? -INFINITY : m + logf(l);
   if (vec) {
     for (int j = 4 * lane; j < N; j += 128) {
-      const float4 x = *reinterpret_cast<const float4*>(s + j);
+      const float4 x = load4(j);
       const uint32_t a = (uint32_t)to16<F16>(allowed(j) ? expf(x.x - L) : 0.f) |
                          ((uint32_t)to16<F16>(allowed(j + 1) ? expf(x.y - L) : 0.f) << 16);
       const uint32_t c = (uint32_t)to16<F16>(allowed(j + 2) ? expf(x.z - L) : 0.f) |
@@ -109,37 +129,38 @@ __global__ void __launch_bounds__(kRowThreads) std_softmax_kernel(const float* _
       *reinterpret_cast<uint2*>(p + j) = make_uint2(a, c);
     }
   } else {
-    for (int j = lane; j < N; j += 32) p[j] = to16<F16>(allowed(j) ? expf(s[j] - L) : 0.f);
+    for (int j = lane; j < N; j += 32) p[j] = to16<F16>(allowed(j) ? expf(load1(j) - L) : 0.f);
   }
   if (lane == 0) lse[row] = L;
 }
 
 // One warp per row: D_i = sum_j P_ij dP_ij, then dS_ij = P_ij (dP_ij - D_i)
 // written over P (the gradient of the softmax, as autograd forms it).
-template <bool F16>
-__global__ void __launch_bounds__(kRowThreads) std_ds_kernel(const float* __restrict__ dP, uint16_t* PdS,
+template <bool F16, bool S16>
+__global__ void __launch_bounds__(kRowThreads) std_ds_kernel(const void* __restrict__ dPv, uint16_t* PdS,
                                                              long long rows, int N) {
   const long long row = (long long)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  const float* g = dP + (size_t)row * N;
   uint16_t* p = PdS + (size_t)row * N;
   const bool vec = (N & 3) == 0;
+  auto load4 = [&](int j) -> float4 { return row_load4<F16, S16>(dPv, (size_t)row * N + j); };
+  auto load1 = [&](int j) -> float { return row_load1<F16, S16>(dPv, (size_t)row * N + j); };
   float acc = 0.f;
   if (vec) {
     for (int j = 4 * lane; j < N; j += 128) {
-      const float4 x = *reinterpret_cast<const float4*>(g + j);
+      const float4 x = load4(j);
       const uint2 pp = *reinterpret_cast<const uint2*>(p + j);
       acc += load16<F16>(pp.x & 0xFFFFu) * x.x + load16<F16>(pp.x >> 16) * x.y +
              load16<F16>(pp.y & 0xFFFFu) * x.z + load16<F16>(pp.y >> 16) * x.w;
     }
   } else {
-    for (int j = lane; j < N; j += 32) acc += load16<F16>(p[j]) * g[j];
+    for (int j = lane; j < N; j += 32) acc += load16<F16>(p[j]) * load1(j);
   }
   const float D = warp_sum(acc);
   if (vec) {
     for (int j = 4 * lane; j < N; j += 128) {
-      const float4 x = *reinterpret_cast<const float4*>(g + j);
+      const float4 x = load4(j);
       const uint2 pp = *reinterpret_cast<const uint2*>(p + j);
       const uint32_t a = (uint32_t)to16<F16>(load16<F16>(pp.x & 0xFFFFu) * (x.x - D)) |
                          ((uint32_t)to16<F16>(load16<F16>(pp.x >> 16) * (x.y - D)) << 16);
@@ -148,7 +169,7 @@ __global__ void __launch_bounds__(kRowThreads) std_ds_kernel(const float* __rest
       *reinterpret_cast<uint2*>(p + j) = make_uint2(a, c);
     }
   } else {
-    for (int j = lane; j < N; j += 32) p[j] = to16<F16>(load16<F16>(p[j]) * (g[j] - D));
+    for (int j = lane; j < N; j += 32) p[j] = to16<F16>(load16<F16>(p[j]) * (load1(j) - D));
   }
 }
 
@@ -230,18 +251,21 @@ size_t standard_attn_workspace_size(int B, int H, int N) {
 
 fa_status standard_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                             int d, float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
-                            const fa_options* options, void* workspace, size_t workspace_bytes, void* stream) {
+                            const fa_options* options, int flags, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   if (!Q || !K || !V || !O || !LSE || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
-      !aligned16(LSE) || (causal != 0 && causal != 1))
+      !aligned16(LSE) || (causal != 0 && causal != 1) || (flags & ~STANDARD_ATTN_S16) != 0)
     return FA_ERR_INVALID_ARG;
+  const bool s16 = (flags & STANDARD_ATTN_S16) != 0;
   bool f16 = false;
   size_t s_bytes = 0;
   fa_status st = check_common(B, H, N, d, scale, options, &f16, workspace, workspace_bytes, &s_bytes);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* S = static_cast<float*>(workspace);
+  void* S = workspace;
   uint16_t* P = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + s_bytes);
   const cudaDataType t16 = f16 ? CUDA_R_16F : CUDA_R_16BF;
+  const cudaDataType ts = s16 ? t16 : CUDA_R_32F;
   const int BH = B * H;
   const long long nd = (long long)N * d, nn = (long long)N * N;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -249,16 +273,20 @@ fa_status standard_attn_fwd(const void* Q, const void* K, const void* V, void* O
   if ((st = cublas_handle(&h)) != FA_OK) return st;
   if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return FA_ERR_CUDA;
   // S = scale * Q K^T  (column-major: S^T = K Q^T)
-  if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, N, N, d, scale, K, t16, d, nd, Q, t16, d, nd, S, CUDA_R_32F, N, nn, BH) !=
+  if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, N, N, d, scale, K, t16, d, nd, Q, t16, d, nd, S, ts, N, nn, BH) !=
       CUBLAS_STATUS_SUCCESS)
     return FA_ERR_CUDA;
   const int nT = (N + kTile - 1) / kTile;
   const long long rows = (long long)BH * N;
   const unsigned grid = (unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta);
-  if (f16)
-    std_softmax_kernel<true><<<grid, kRowThreads, 0, s>>>(S, P, LSE, rows, H, N, nT, causal, kv_len, block_mask);
-  else
-    std_softmax_kernel<false><<<grid, kRowThreads, 0, s>>>(S, P, LSE, rows, H, N, nT, causal, kv_len, block_mask);
+#define STD_SOFTMAX(FF, SS) \
+  std_softmax_kernel<FF, SS><<<grid, kRowThreads, 0, s>>>(S, P, LSE, rows, H, N, nT, causal, kv_len, block_mask)
+  if (f16) {
+    if (s16) STD_SOFTMAX(true, true); else STD_SOFTMAX(true, false);
+  } else {
+    if (s16) STD_SOFTMAX(false, true); else STD_SOFTMAX(false, false);
+  }
+#undef STD_SOFTMAX
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   // O = P V  (column-major: O^T = V^T P^T)
   if (gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, d, N, N, 1.f, V, t16, d, nd, P, t16, N, nn, O, t16, d, nd, BH) !=
@@ -269,18 +297,20 @@ fa_status standard_attn_fwd(const void* Q, const void* K, const void* V, void* O
 
 fa_status standard_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, void* dQ, void* dK,
                             void* dV, int B, int H, int N, int d, float scale, const fa_options* options,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+                            int flags, void* workspace, size_t workspace_bytes, void* stream) {
   if (!Q || !K || !V || !dO || !dQ || !dK || !dV || !aligned16(Q) || !aligned16(K) || !aligned16(V) ||
-      !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+      !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) || (flags & ~STANDARD_ATTN_S16) != 0)
     return FA_ERR_INVALID_ARG;
+  const bool s16 = (flags & STANDARD_ATTN_S16) != 0;
   bool f16 = false;
   size_t s_bytes = 0;
   fa_status st = check_common(B, H, N, d, scale, options, &f16, workspace, workspace_bytes, &s_bytes);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* dP = static_cast<float*>(workspace);
+  void* dP = workspace;
   uint16_t* P = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + s_bytes);
   const cudaDataType t16 = f16 ? CUDA_R_16F : CUDA_R_16BF;
+  const cudaDataType ts = s16 ? t16 : CUDA_R_32F;
   const int BH = B * H;
   const long long nd = (long long)N * d, nn = (long long)N * N;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -292,15 +322,18 @@ fa_status standard_attn_bwd(const void* Q, const void* K, const void* V, const v
       CUBLAS_STATUS_SUCCESS)
     return FA_ERR_CUDA;
   // dP = dO V^T  (column-major: dP^T = V dO^T)
-  if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, N, N, d, 1.f, V, t16, d, nd, dO, t16, d, nd, dP, CUDA_R_32F, N, nn, BH) !=
+  if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, N, N, d, 1.f, V, t16, d, nd, dO, t16, d, nd, dP, ts, N, nn, BH) !=
       CUBLAS_STATUS_SUCCESS)
     return FA_ERR_CUDA;
   const long long rows = (long long)BH * N;
   const unsigned grid = (unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta);
-  if (f16)
-    std_ds_kernel<true><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
-  else
-    std_ds_kernel<false><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
+  if (f16) {
+    if (s16) std_ds_kernel<true, true><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
+    else std_ds_kernel<true, false><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
+  } else {
+    if (s16) std_ds_kernel<false, true><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
+    else std_ds_kernel<false, false><<<grid, kRowThreads, 0, s>>>(dP, P, rows, N);
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const uint16_t* dS = P;
   // dQ = scale * dS K  (column-major: dQ^T = K^T dS^T)

@@ -22,7 +22,8 @@
  *  - d may be any multiple of 8 from 8 to 256;
  *  - the workspace holds the materialised matrices and carries P from
  *    standard_attn_fwd to standard_attn_bwd:
- *      S (fp32 [B, H, N, N]; reused for dP in the backward pass), then
+ *      S (fp32 [B, H, N, N], or 16-bit with STANDARD_ATTN_S16; reused for dP
+ *      in the backward pass), then
  *      P (16-bit [B, H, N, N]; overwritten in place by dS in the backward
  *      pass, so a second backward call needs a new forward call);
  *  - cuBLAS may allocate its own workspace when the library creates its
@@ -38,8 +39,22 @@ extern "C" {
 #endif
 
 /* Bytes of workspace for this shape (fp32 S plus 16-bit P, each section
- * 256-byte aligned); 0 for an invalid shape or one whose size overflows. */
+ * 256-byte aligned; enough for either flag setting); 0 for an invalid shape
+ * or one whose size overflows. */
 size_t standard_attn_workspace_size(int B, int H, int N);
+
+/*
+ * flags of standard_attn_fwd / standard_attn_bwd:
+ *   STANDARD_ATTN_S16: S = scale * Q K^T and dP = dO V^T are stored in the
+ *   16-bit element type of the inputs (as a framework's 16-bit matmul
+ *   returns them) instead of fp32; the softmax and dS still compute in fp32
+ *   from the stored values. This is the low-precision standard attention the
+ *   pages' stability remark is about (FlashAttention proof-of-work page, the
+ *   question whether the method is an approximation: with its online softmax
+ *   and high-precision accumulators it is often numerically more stable than
+ *   standard PyTorch attention). fwd and bwd must use the same flags.
+ */
+#define STANDARD_ATTN_S16 1
 
 /*
  * Forward pass: writes S and P to the workspace, then O and LSE.
@@ -50,14 +65,15 @@ size_t standard_attn_workspace_size(int B, int H, int N);
  *   causal 0 or 1; kv_len, block_mask as in flash_attn.h (may be NULL).
  *   options: NULL or an fa_options; only dtype is used, p_drop must be 0
  *            (FA_ERR_UNSUPPORTED otherwise).
+ *   flags:   0 or STANDARD_ATTN_S16 (FA_ERR_INVALID_ARG otherwise).
  *   workspace: at least standard_attn_workspace_size(B, H, N) bytes,
  *            256-byte aligned (FA_ERR_WORKSPACE otherwise).
  */
 fa_status standard_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                             int B, int H, int N, int d, float scale, int causal,
                             const int32_t* kv_len, const uint8_t* block_mask,
-                            const fa_options* options, void* workspace, size_t workspace_bytes,
-                            void* stream);
+                            const fa_options* options, int flags, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass from the P that standard_attn_fwd left in the workspace:
@@ -69,8 +85,8 @@ fa_status standard_attn_fwd(const void* Q, const void* K, const void* V, void* O
  */
 fa_status standard_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
                             void* dQ, void* dK, void* dV, int B, int H, int N, int d, float scale,
-                            const fa_options* options, void* workspace, size_t workspace_bytes,
-                            void* stream);
+                            const fa_options* options, int flags, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

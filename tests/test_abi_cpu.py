@@ -117,12 +117,14 @@ def test_standard_attn_arguments_validated_before_any_launch(lib):
     p = ctypes.c_void_p(1 << 20)
     bad = ctypes.c_void_p((1 << 20) + 8)
     ws = L.standard_attn_workspace_size(1, 1, 128)
-    def fwd(*, d=64, N=128, causal=0, opts=None, w=p, nbytes=ws, q=p, scale=0.1):
-        return L.standard_attn_fwd(q, p, p, p, p, 1, 1, N, d, scale, causal, None, None, opts, w, nbytes, None)
+    def fwd(*, d=64, N=128, causal=0, opts=None, w=p, nbytes=ws, q=p, scale=0.1, flags=0):
+        return L.standard_attn_fwd(q, p, p, p, p, 1, 1, N, d, scale, causal, None, None, opts, flags, w, nbytes,
+                                   None)
     assert fwd(q=None) == 1 and fwd(q=bad) == 1 and fwd(causal=2) == 1 and fwd(scale=float("nan")) == 1
-    assert fwd(d=60) == 2 and fwd(d=264) == 2 and fwd(N=65537) == 2
+    assert fwd(d=60) == 2 and fwd(d=264) == 2 and fwd(N=65537) == 2 and fwd(flags=2) == 1
     assert fwd(opts=L.fa_options(p_drop=0.1)) == 2        # dropout is not part of the baseline
     assert fwd(opts=L.fa_options(7)) == 2
     assert fwd(nbytes=ws - 1) == 3 and fwd(w=None) == 3 and fwd(w=ctypes.c_void_p((1 << 20) + 16)) == 3
-    assert L.standard_attn_bwd(p, p, p, p, p, p, None, 1, 1, 128, 64, 0.1, None, p, ws, None) == 1
-    assert L.standard_attn_bwd(p, p, p, p, p, p, p, 1, 1, 128, 64, 0.1, None, p, ws - 1, None) == 3
+    assert L.standard_attn_bwd(p, p, p, p, p, p, None, 1, 1, 128, 64, 0.1, None, 0, p, ws, None) == 1
+    assert L.standard_attn_bwd(p, p, p, p, p, p, p, 1, 1, 128, 64, 0.1, None, 0, p, ws - 1, None) == 3
+    assert L.standard_attn_bwd(p, p, p, p, p, p, p, 1, 1, 128, 64, 0.1, None, 5, p, ws, None) == 1
