@@ -333,13 +333,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
         }
       }
+      // row max with three-input max: 8 independent chains over 128 scores
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = x[k];
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int i = 8; i < 120; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], x[i + k], x[i + 8 + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[120 + k]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_new = mx * sl2;
       // move the reference max only when the row max grew by more than the
       // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
@@ -364,7 +368,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         tmem_st_wait();
       }
       const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // packed fp32 pairs (one f32x2 instruction per two keys) for the
+      // exponent arguments and the row sum: the softmax is issue-bound
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 nref2 = make_float2(-ref, -ref);
+      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
       // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4
       const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
@@ -374,9 +382,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(x[64 * hh + 2 * i], sl2, -ref));
-          const float p1 = ex2(fmaf(x[64 * hh + 2 * i + 1], sl2, -ref));
-          sum8[i & 7] += p0 + p1;   // the statistics use the undropped P
+          const float2 a = __ffma2_rn(make_float2(x[64 * hh + 2 * i], x[64 * hh + 2 * i + 1]), sl2x2, nref2);
+          const float p0 = ex2(a.x);
+          const float p1 = ex2(a.y);
+          sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
           if constexpr (DROP) {
             if ((i & 1) == 0)
               rw = uint4_word(philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1),
@@ -393,7 +402,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         tmem_st32(tS + 32u * hh, pk);
       }
       tmem_st_wait();
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
+      const float2 s4 = __fadd2_rn(s01, s23);
+      l += s4.x + s4.y;
       tc_fence_before();
       mbar_arrive_warp(bar(L::bPFull + t));
       ++n;

@@ -383,6 +383,13 @@ __device__ __forceinline__ void regs_dec() {
 // arithmetic helpers
 // ---------------------------------------------------------------------------
 
+// max of three (the three-input form of PTX max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
