@@ -21,8 +21,12 @@
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
 //        dK  += dS^T Q         (A = dS^T from TMEM, B = Q MN-major)
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
-//      S^T of the next query tile is issued after dK and dQ of the current one,
-//      which leaves its Q load the longest window.
+//      At d = 128, S^T of the next query tile is issued after dK and dQ of
+//      the current one, which leaves its Q load the longest window (the dQ
+//      partial reuses the dP^T columns, so the next dP^T waits for its drain;
+//      S^T runs meanwhile). At d = 64 the dQ partial has TMEM columns of its
+//      own and S^T of the next tile follows dV directly, so that P of the
+//      next tile is recomputed while dK, dQ and the next dP^T run.
 //      Each dQ partial is drained from TMEM into shared memory (the dO ring
 //      slot of its own query tile, dead once dQ is issued, in two rounds) and
 //      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
@@ -155,7 +159,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t tdV = tmem;
   const uint32_t tdK = tmem + (uint32_t)D;
   const uint32_t tS = tmem + 2u * D;
-  const uint32_t tP = tmem + 2u * D + 128u;   // dP^T, then the dQ partial
+  const uint32_t tP = tmem + 2u * D + 128u;   // dP^T (and at d = 128 then the dQ partial)
+  // At d = 64 the dQ partial has 64 columns of its own (2d + 256 + d <= 512),
+  // which allows a schedule where nothing waits for its drain (see the MMA
+  // issuer); at d = 128 it reuses the dP^T columns.
+  constexpr bool kOwnDQ = (D == 64);
+  const uint32_t tQ = kOwnDQ ? tmem + 2u * D + 256u : tP;
+  // dS^T for dK: packed into the S columns next to P^T at d = 128 (S^T of the
+  // next tile is issued after dK), into the dP^T columns at d = 64 (S^T of
+  // the next tile is issued before dK)
+  const uint32_t tDS = kOwnDQ ? tP : tS + 32u;
 
   if (warp >= 12) regs_dec<kOtherRegs>();
   if (warp == kProducerWarp) {
@@ -220,12 +233,26 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sbase + L::kQ, ks), idSP, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bSFull));
       }
+      // S^T of the query tile after `it` (none after the last)
+      auto issue_next_s = [&](int it) -> bool {
+        if (it + 1 >= len) return true;
+        const int s1 = (it + 1) % L::kStages;
+        if (!mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114)) return false;
+        tc_fence_after();
+        const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
+        mma_commit(bar(L::bSFull));
+        return true;
+      };
       for (int it = 0; it < len && ok; ++it) {
         const int s = it % L::kStages;
         const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
         const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
-        // dP^T = V dO^T (the dQ partial of the previous tile must have been read out)
-        if (it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
+        // dP^T = V dO^T (at d = 128 the dQ partial of the previous tile must
+        // have been read out of these columns)
+        if (!kOwnDQ && it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
         if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 116))) break;
         tc_fence_after();
 #pragma unroll
@@ -240,32 +267,29 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
           mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sdO, ks), idV,
                  (it > 0 || ks > 0) ? 1u : 0u);
+        // next S^T: at d = 64 right behind dV (the tensor pipe runs in issue
+        // order, so dV has read P first), so that P of the next tile is
+        // recomputed while dK, dQ and the next dP run; at d = 128 after dQ,
+        // which leaves the next Q load the longest window
+        if (kOwnDQ && !(ok = issue_next_s(it))) break;
         // dK += dS^T Q ; dQ_i = dS K
         if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)it & 1u, ctl, 115))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          // dS^T of queries 0-63 in S columns 32-63, of queries 64-127 in 96-127
-          mma_ts(tdK, tS + 32u + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
+          // dS^T of queries 0-63 in columns tDS + 0..31, of queries 64-127 in tDS + 64..95
+          mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
                  (it > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
+        // at d = 64 the previous dQ partial must have been read out of its columns
+        if (kOwnDQ && it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tP, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
+          mma_ss(tQ, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bdQFull));
         mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
-        // next S^T (after this tile's dK and dQ: a longer window for its Q load)
-        if (it + 1 < len) {
-          const int s1 = (it + 1) % L::kStages;
-          if (!(ok = mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114))) break;
-          tc_fence_after();
-          const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
-          mma_commit(bar(L::bSFull));
-        }
-
+        if (!kOwnDQ && !(ok = issue_next_s(it))) break;
       }
       mma_commit(bar(L::bFinal));
       mma_commit(bar(L::bDrain));
@@ -381,9 +405,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const float d1 = x[c0 + 1] * (g1 - dl.y);
           pk[c] = pack2<F16>(d0, d1);
         }
-        // dS^T also goes to TMEM (the A operand of dK): the second half of this
-        // warpgroup's S columns, after its P
-        tmem_st16(tS + lane_off + 32u + (uint32_t)cb + 16u * cc, pk);
+        // dS^T also goes to TMEM (the A operand of dK), packed: at d = 128 into
+        // the second half of this warpgroup's S columns, after its P; at d = 64
+        // over this warpgroup's dP columns, which it has already read
+        tmem_st16(tDS + lane_off + (uint32_t)cb + 16u * cc, pk);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint8_t* dst = smem + L::kdS + swz_off(r, cb + 32 * cc + 8 * k);
@@ -455,7 +480,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tc_fence_after();
       uint32_t u[kBoxesPerRound][32];
 #pragma unroll
-      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld32(tP + lane_off + 32u * b, u[b]);
+      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld32(tQ + lane_off + 32u * b, u[b]);
 #pragma unroll
       for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
 #pragma unroll
@@ -488,7 +513,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (round + 1 < kRounds) {    // the next columns into registers while the round is read
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b)
-            tmem_ld32(tP + lane_off + 32u * ((round + 1) * kBoxesPerRound + b), u[b]);
+            tmem_ld32(tQ + lane_off + 32u * ((round + 1) * kBoxesPerRound + b), u[b]);
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
         }
