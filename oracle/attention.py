@@ -117,6 +117,43 @@ def head_backward(q, k, v, do, scale, P, O):
     return dict(dP=dP, D=D, dS=dS, dQ=dQ, dK=dK, dV=dV)
 
 
+def head_rows(q, k, v, do, scale, causal, rows, keys, chunk=64):
+    """Selected outputs of one head, float64, for lengths whose N x N matrices
+    do not fit: O, LSE and dQ of the query rows ``rows``, dK and dV of the key
+    rows ``keys``. The same definition as head_forward / head_backward,
+    evaluated for blocks of query rows at a time (only the causal mask).
+
+    A key's gradient sums over every query row that may attend to it: with
+    causal masking those are the rows at or after the key, so keys near the
+    end need few rows; without it every row is visited.
+    Returns dict(O [len(rows), d], LSE [len(rows)], dQ [len(rows), d],
+    dK [len(keys), d], dV [len(keys), d]).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    N, d = q.shape
+    rows = [int(i) for i in rows]
+    keys = [int(j) for j in keys]
+    first = min(keys) if (keys and causal) else 0
+    need = sorted(set(rows) | (set(range(first, N)) if keys else set()))
+    pos = {i: n for n, i in enumerate(rows)}
+    out = dict(O=np.zeros((len(rows), d)), LSE=np.zeros(len(rows)), dQ=np.zeros((len(rows), d)),
+               dK=np.zeros((len(keys), d)), dV=np.zeros((len(keys), d)))
+    kj = np.array(keys, dtype=np.int64)
+    for c0 in range(0, len(need), chunk):
+        I = np.array(need[c0:c0 + chunk], dtype=np.int64)
+        allowed = (np.arange(N)[None, :] <= I[:, None]) if causal else np.ones((len(I), N), bool)
+        f = head_forward(q[I], k, v, scale, allowed)
+        g = head_backward(q[I], k, v, do[I], scale, f["P"], f["O"])
+        for n, i in enumerate(I):
+            if int(i) in pos:
+                r = pos[int(i)]
+                out["O"][r], out["LSE"][r], out["dQ"][r] = f["O"][n], f["LSE"][n], g["dQ"][n]
+        if len(keys):
+            out["dV"] += f["P"][:, kj].T @ do[I]
+            out["dK"] += scale * (g["dS"][:, kj].T @ q[I])
+    return out
+
+
 def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None,
                   heads=None):
     """Batched forward on [B, H, N, d] inputs.

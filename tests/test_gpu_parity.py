@@ -167,6 +167,36 @@ def test_head_dim_96_fp16(fa):
     _compare(got, ref, o_rel=HEAD_DIM_O_REL)
 
 
+MAX_LEN = [
+    # the longest supported sequence (131072 keys), and a ragged length just below it
+    (131072, 64),
+    (131071, 128),
+]
+
+
+@pytest.mark.parametrize("N,d", MAX_LEN, ids=[f"N{n}_d{d}" for n, d in MAX_LEN])
+def test_maximum_length_sampled_rows(fa, N, d):
+    """Causal attention at the maximum length, compared on sampled query rows
+    (O, LSE, dQ) and on key rows near the end (dK, dV: under the causal mask
+    they need only the rows after them), computed by the oracle row block by
+    row block. O bound as for the head-dimension cases (early causal rows
+    average two or three values, |O| > 2.5)."""
+    c = _small_case(f"maxlen_{N}_{d}", 1, 1, N, d, True, None, None)
+    got = _run_gpu(fa, c)
+    rows = [0, 1, 127, 128, 4097, N // 2, N - 129, N - 1]
+    keys = [N - 1, N - 2, N - 130, N - 300]
+    ref = oracle.head_rows(c["q"][0, 0], c["k"][0, 0], c["v"][0, 0], c["do"][0, 0], c["scale"], True,
+                           rows, keys)
+    o_ref = ref["O"]
+    o_got = got["O"][0, 0][rows]
+    assert (np.abs(o_got - o_ref) - HEAD_DIM_O_REL * np.abs(o_ref)).max() <= O_TOL
+    assert np.abs(got["LSE"][0, 0][rows] - ref["LSE"]).max() <= LSE_TOL
+    for name, idx in (("dQ", rows), ("dK", keys), ("dV", keys)):
+        g, r = got[name][0, 0][idx], ref[name]
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert rel <= GRAD_TOL, (name, rel)
+
+
 @pytest.mark.parametrize("spec", SMALL, ids=[s[0] for s in SMALL])
 def test_tile_map_bit_exact(fa, spec):
     c = _small_case(*spec)

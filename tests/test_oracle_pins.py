@@ -345,3 +345,18 @@ def test_planted_gradient_mistakes_are_caught(bad):
     r = bad(q, k, v, do, scale, f["P"], f["O"])
     worst = max(_rel(r["dQ"], fdq), _rel(r["dK"], fdk), _rel(r["dV"], fdv))
     assert worst > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_equal_the_full_oracle(causal):
+    """head_rows (used where the N x N matrices do not fit) against the full
+    oracle on a length that fits: the same values to rounding."""
+    from oracle import attention as oa
+    rng = np.random.default_rng(21)
+    N, d, scale = 300, 16, 0.3
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    ref = oa.attention_fwd_bwd(q[None, None], k[None, None], v[None, None], do[None, None], scale, causal)
+    rows, keys = [0, 1, 129, 250, 299], [299, 290, 200]
+    got = oa.head_rows(q, k, v, do, scale, causal, rows, keys)
+    for name, idx in (("O", rows), ("LSE", rows), ("dQ", rows), ("dK", keys), ("dV", keys)):
+        np.testing.assert_allclose(got[name], ref[name][0, 0][idx], rtol=1e-12, atol=1e-12, err_msg=name)
