@@ -24,9 +24,10 @@
 //   * O_t accumulates in TMEM for the whole K/V sweep and is written once;
 //   * the two Q tiles ping-pong: while one softmax group works on its S, the
 //     tensor core runs the other tile's P V and next S;
-//   * the MMA thread is event driven: each Q tile walks only its own live key
-//     tiles (causal, key-length and block-sparse skipping are exact per tile),
-//     while K/V tiles are loaded once for the pair.
+//   * the MMA thread follows a fixed schedule over the union list of key
+//     tiles live for either Q tile (causal, key-length and block-sparse
+//     skipping are exact per tile), while K/V tiles are loaded once for the
+//     pair.
 //   * the running max is moved (and O rescaled) only when a new row max
 //     exceeds it by more than 2^8; the final O / l and LSE use the same
 //     reference max, so the result is unchanged.
