@@ -457,7 +457,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       for (int h = 0; h < L::kHalves; ++h)
         tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + (cw == 0 ? L::kV : L::kK) + h * 16384, 64 * h, kTile * kj, bh);
       bulk_commit_group();
-      bulk_wait_group_all();
+      bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)

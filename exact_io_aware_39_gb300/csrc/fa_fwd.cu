@@ -456,7 +456,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int h = 0; h < L::kHalves; ++h)
           tma_store_3d(&to, smem_u32(stage) + h * 16384, 64 * h, kTile * qi, bh);
         bulk_commit_group();
-        bulk_wait_group_all();
+        bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
       }
     }
   }
