@@ -60,15 +60,17 @@ struct BwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kHalves = D / 64;
   static constexpr int kStages = (D == 64) ? 3 : 2;   // Q/dO ring depth (smem-limited at d = 128)
-  static constexpr int kK = 0;
+  static constexpr int kKV = (D == 64) ? 2 : 1;        // K/V buffers (a second one fits at d = 64)
+  static constexpr int kKVBytes = 2 * kTileBytes;
+  static constexpr int kK = 0;                                // [kKV] buffers of K then V
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;                  // [stages]
+  static constexpr int kQ = kKV * kKVBytes;                   // [stages]
   static constexpr int kdO = kQ + kStages * kTileBytes;       // [stages]
   static constexpr int kdS = kdO + kStages * kTileBytes;      // 128 x 128 bf16
   static constexpr int kRow = kdS + kTile * kTile * 2;        // [stages] x (LSE2[128], D[128])
   static constexpr int kBar = kRow + kStages * 2 * kTile * 4;
-  static constexpr int bKV = 0;
-  static constexpr int bQFull = 1;
+  static constexpr int bKV = 0;                            // [kKV]
+  static constexpr int bQFull = bKV + kKV;
   static constexpr int bQEmpty = bQFull + kStages;
   static constexpr int bdOFull = bQEmpty + kStages;        // [stages]
   static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA
@@ -81,7 +83,8 @@ struct BwdLayout {
   static constexpr int bdQFree = bdQFull + 1;
   static constexpr int bFinal = bdQFree + 1;
   static constexpr int bDrain = bFinal + 1;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (2 arrivals)
+  static constexpr int kNumBars = bKVFree + kKV;
   static constexpr int kMisc = kBar + 8 * kNumBars;
   static constexpr int kSmemBytes = kMisc + 16;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -111,17 +114,33 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   const int BH = p.B * p.H;
   const int Np = p.nT * kTile;
-  const int kj = blockIdx.x / BH;          // low key tiles (most live query tiles) first
-  const int bh = blockIdx.x % BH;
-  const int b = bh / p.H;
-  const int kvl = effective_kv_len(p.kv_len, b, p.N);
+  // Work items are (key tile, batch-head) pairs, L = kj * BH + bh, low key
+  // tiles (the most live query tiles) first. A CTA takes item
+  // k * gridDim.x + (its index, or the mirrored index on odd k): the rounds
+  // alternate direction so that the CTAs' shares of long and short items
+  // balance.
+  const int total = p.nT * BH;
+  auto item_index = [&](int k) -> int {
+    const int pos = (k & 1) ? (int)(gridDim.x - 1u - blockIdx.x) : (int)blockIdx.x;
+    return k * (int)gridDim.x + pos;
+  };
+  struct Item {
+    int kj, bh, kvl;   // key tile, batch-head, key length of the batch entry
+  };
+  auto item_at = [&](int item) -> Item {
+    Item w;
+    w.kj = item / BH;
+    w.bh = item % BH;
+    w.kvl = effective_kv_len(p.kv_len, w.bh / p.H, p.N);
+    return w;
+  };
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
-  // live query tiles of this key tile, visited in ascending order by every role
-  auto next_live = [&](int i) -> int {
-    while (i < p.nT && tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) == kSkip) ++i;
+  // live query tiles of an item's key tile, visited in ascending order by every role
+  auto next_live = [&](const Item& w, int i) -> int {
+    while (i < p.nT && tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kSkip) ++i;
     return i;
   };
   Ctl ctl{p.err, abort_flag};
@@ -137,7 +156,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u : (i == L::bdQFree ? 4u : 1u));   // warps
+      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u
+                        : i == L::bdQFree ? 4u : i >= L::bKVFree ? 2u : 1u);   // arrivals
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -145,17 +165,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    int count = 0;
-    for (int i = 0; i < p.nT; ++i) count += tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) != kSkip;
-    misc[2] = (uint32_t)count;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   const uint32_t tmem = misc[0];
-  const int len = (int)misc[2];
   const uint32_t tdV = tmem;
   const uint32_t tdK = tmem + (uint32_t)D;
   const uint32_t tS = tmem + 2u * D;
@@ -170,6 +184,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // the next tile is issued before dK)
   const uint32_t tDS = kOwnDQ ? tP : tS + 32u;
 
+  // Every role walks the same items in the same order and counts the live
+  // query tiles it has passed over all of them (g): ring slots and barrier
+  // phases follow g, so the pipeline runs on across item boundaries.
   if (warp >= 12) regs_dec<kOtherRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -178,66 +195,83 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tma_prefetch_map(&tk);
       tma_prefetch_map(&tv);
       tma_prefetch_map(&tdo);
-      mbar_arrive_expect_tx(bar(L::bKV), 2u * L::kTileBytes);
-      for (int h = 0; h < L::kHalves; ++h) {
-        tma_load_3d(sbase + L::kK + h * 16384, &tk, bar(L::bKV), 64 * h, kTile * kj, bh);
-        tma_load_3d(sbase + L::kV + h * 16384, &tv, bar(L::bKV), 64 * h, kTile * kj, bh);
+      int nq = 0, nd = 0, nkv = 0;
+      // K and V of item k into buffer k % kKV, once the epilogue of the item
+      // that used the buffer before has been read out of it; a key tile with
+      // no live query tile loads nothing (its epilogue stores zeros)
+      auto load_kv = [&](int k, const Item& w, bool live) -> bool {
+        const int kb = k % L::kKV;
+        if (k >= L::kKV && !mbar_wait(bar(L::bKVFree + kb), (uint32_t)(k / L::kKV - 1) & 1u, ctl, 103)) return false;
+        if (live) {
+          mbar_arrive_expect_tx(bar(L::bKV + kb), 2u * L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h) {
+            tma_load_3d(sbase + L::kK + kb * L::kKVBytes + h * 16384, &tk, bar(L::bKV + kb), 64 * h, kTile * w.kj, w.bh);
+            tma_load_3d(sbase + L::kV + kb * L::kKVBytes + h * 16384, &tv, bar(L::bKV + kb), 64 * h, kTile * w.kj, w.bh);
+          }
+        } else {
+          mbar_arrive(bar(L::bKV + kb));
+        }
+        ++nkv;
+        return true;
+      };
+      bool ok = true;
+      int g = 0;
+      for (int k = 0; ok; ++k) {
+        const int item = item_index(k);
+        if (item >= total) break;
+        const Item w = item_at(item);
+        int i = next_live(w, 0);
+        if (i >= p.nT) {
+          ok = load_kv(k, w, false);
+          continue;
+        }
+        for (int it = 0; i < p.nT; ++it, ++g, i = next_live(w, i + 1)) {
+          const int s = g % L::kStages;
+          const uint32_t n = (uint32_t)(g / L::kStages);
+          // Q and the row statistics once dK has read the slot's Q; dO once the
+          // dQ partial staged in the slot's dO buffer has been read
+          if (g >= L::kStages && !(ok = mbar_wait(bar(L::bQEmpty + s), (n - 1) & 1u, ctl, 101))) break;
+          mbar_arrive_expect_tx(bar(L::bQFull + s), L::kTileBytes + 2u * kTile * 4u);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kQ + s * L::kTileBytes + h * 16384, &tq, bar(L::bQFull + s),
+                        64 * h, kTile * i, w.bh);
+          const size_t roff = (size_t)w.bh * Np + (size_t)kTile * i;
+          bulk_load(sbase + L::kRow + s * 1024, p.lse2 + roff, kTile * 4, bar(L::bQFull + s));
+          bulk_load(sbase + L::kRow + s * 1024 + 512, p.delta + roff, kTile * 4, bar(L::bQFull + s));
+          ++nq;
+          if (g >= L::kStages && !(ok = mbar_wait(bar(L::bdOFree + s), (n - 1) & 1u, ctl, 102))) break;
+          mbar_arrive_expect_tx(bar(L::bdOFull + s), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kdO + s * L::kTileBytes + h * 16384, &tdo, bar(L::bdOFull + s),
+                        64 * h, kTile * i, w.bh);
+          ++nd;
+          // K and V behind the first query tile of the item, whose loads only
+          // wait for ring slots of the previous item
+          if (it == 0 && !(ok = load_kv(k, w, true))) break;
+        }
       }
-      int nq = 0, nd = 0;
-      int i = next_live(0);
-      for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
-        const int s = it % L::kStages;
-        const uint32_t n = (uint32_t)(it / L::kStages);
-        // Q and the row statistics once dK has read the slot's Q; dO once the
-        // dQ partial staged in the slot's dO buffer has been read
-        if (it >= L::kStages && !mbar_wait(bar(L::bQEmpty + s), (n - 1) & 1u, ctl, 101)) break;
-        mbar_arrive_expect_tx(bar(L::bQFull + s), L::kTileBytes + 2u * kTile * 4u);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kQ + s * L::kTileBytes + h * 16384, &tq, bar(L::bQFull + s),
-                      64 * h, kTile * i, bh);
-        const size_t roff = (size_t)bh * Np + (size_t)kTile * i;
-        bulk_load(sbase + L::kRow + s * 1024, p.lse2 + roff, kTile * 4, bar(L::bQFull + s));
-        bulk_load(sbase + L::kRow + s * 1024 + 512, p.delta + roff, kTile * 4, bar(L::bQFull + s));
-        ++nq;
-        if (it >= L::kStages && !mbar_wait(bar(L::bdOFree + s), (n - 1) & 1u, ctl, 102)) break;
-        mbar_arrive_expect_tx(bar(L::bdOFull + s), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kdO + s * L::kTileBytes + h * 16384, &tdo, bar(L::bdOFull + s),
-                      64 * h, kTile * i, bh);
-        ++nd;
-      }
-      drain_wait(bar(L::bKV), 0);
-      for (int s = 0; s < L::kStages; ++s)
-      {
-        if (s < nq)
-          drain_wait(bar(L::bQFull + s),
-                     (uint32_t)((s + ((nq - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
-        if (s < nd)
-          drain_wait(bar(L::bdOFull + s),
-                     (uint32_t)((s + ((nd - 1 - s) / L::kStages) * L::kStages) / L::kStages) & 1u);
+      // every load issued has landed before the CTA exits
+      for (int kb = 0; kb < L::kKV && kb < nkv; ++kb)
+        drain_wait(bar(L::bKV + kb), (uint32_t)((nkv - 1 - kb) / L::kKV) & 1u);
+      for (int s = 0; s < L::kStages; ++s) {
+        if (s < nq) drain_wait(bar(L::bQFull + s), (uint32_t)((nq - 1 - s) / L::kStages) & 1u);
+        if (s < nd) drain_wait(bar(L::bdOFull + s), (uint32_t)((nd - 1 - s) / L::kStages) & 1u);
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && len > 0) {
+    if (lane == 0) {
       constexpr uint32_t idSP = idesc_16<F16>(128, 128, false, false);
       constexpr uint32_t idV = idesc_16<F16>(128, D, false, true);
       constexpr uint32_t idK = idesc_16<F16>(128, D, false, true);
       constexpr uint32_t idQ = idesc_16<F16>(128, D, true, true);
-      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sdS = sbase + L::kdS;
-      bool ok = mbar_wait(bar(L::bKV), 0, ctl, 110) && mbar_wait(bar(L::bQFull), 0, ctl, 111);
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sbase + L::kQ, ks), idSP, ks > 0 ? 1u : 0u);
-        mma_commit(bar(L::bSFull));
-      }
-      // S^T of the query tile after `it` (none after the last)
-      auto issue_next_s = [&](int it) -> bool {
-        if (it + 1 >= len) return true;
-        const int s1 = (it + 1) % L::kStages;
-        if (!mbar_wait(bar(L::bQFull + s1), (uint32_t)((it + 1) / L::kStages) & 1u, ctl, 114)) return false;
+      const uint32_t sdS = sbase + L::kdS;
+      bool ok = true;
+      int g = 0;
+      // S^T = K Q^T of running query tile g
+      auto issue_s = [&](uint32_t sK, int g1) -> bool {
+        const int s1 = g1 % L::kStages;
+        if (!mbar_wait(bar(L::bQFull + s1), (uint32_t)(g1 / L::kStages) & 1u, ctl, 114)) return false;
         tc_fence_after();
         const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
 #pragma unroll
@@ -246,52 +280,66 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mma_commit(bar(L::bSFull));
         return true;
       };
-      for (int it = 0; it < len && ok; ++it) {
-        const int s = it % L::kStages;
-        const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
-        const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
-        // dP^T = V dO^T (at d = 128 the dQ partial of the previous tile must
-        // have been read out of these columns)
-        if (!kOwnDQ && it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
-        if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 116))) break;
-        tc_fence_after();
+      for (int k = 0; ok; ++k) {
+        const int item = item_index(k);
+        if (item >= total) break;
+        const Item w = item_at(item);
+        int i = next_live(w, 0);
+        if (i >= p.nT) continue;
+        const int kb = k % L::kKV;
+        const uint32_t sK = sbase + L::kK + kb * L::kKVBytes, sV = sbase + L::kV + kb * L::kKVBytes;
+        if (!(ok = mbar_wait(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 110))) break;
+        if (!(ok = issue_s(sK, g))) break;
+        for (int it = 0; i < p.nT; ++it, ++g) {
+          const int inext = next_live(w, i + 1);
+          const int s = g % L::kStages;
+          const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
+          const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
+          // dP^T = V dO^T (at d = 128 the dQ partial of the previous tile must
+          // have been read out of these columns)
+          if (!kOwnDQ && g > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
+          if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 116))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tP, desc_kmajor(sV, ks), desc_kmajor(sdO, ks), idSP, ks > 0 ? 1u : 0u);
-        mma_commit(bar(L::bdPFull));
-        // dV += P^T dO
-        if (!(ok = mbar_wait(bar(L::bPFull), (uint32_t)it & 1u, ctl, 113))) break;
-        tc_fence_after();
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tP, desc_kmajor(sV, ks), desc_kmajor(sdO, ks), idSP, ks > 0 ? 1u : 0u);
+          mma_commit(bar(L::bdPFull));
+          // dV += P^T dO (at it == 0 over the previous item's dV and dK, which
+          // the compute warps have read out of TMEM before arriving on this P)
+          if (!(ok = mbar_wait(bar(L::bPFull), (uint32_t)g & 1u, ctl, 113))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
-          mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sdO, ks), idV,
-                 (it > 0 || ks > 0) ? 1u : 0u);
-        // next S^T: at d = 64 right behind dV (the tensor pipe runs in issue
-        // order, so dV has read P first), so that P of the next tile is
-        // recomputed while dK, dQ and the next dP run; at d = 128 after dQ,
-        // which leaves the next Q load the longest window
-        if (kOwnDQ && !(ok = issue_next_s(it))) break;
-        // dK += dS^T Q ; dQ_i = dS K
-        if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)it & 1u, ctl, 115))) break;
-        tc_fence_after();
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
+            mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sdO, ks), idV,
+                   (it > 0 || ks > 0) ? 1u : 0u);
+          // next S^T of this item: at d = 64 right behind dV (the tensor pipe
+          // runs in issue order, so dV has read P first), so that P of the
+          // next tile is recomputed while dK, dQ and the next dP run; at
+          // d = 128 after dQ, which leaves the next Q load the longest window
+          if (kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
+          // dK += dS^T Q ; dQ_i = dS K
+          if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)g & 1u, ctl, 115))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          // dS^T of queries 0-63 in columns tDS + 0..31, of queries 64-127 in tDS + 64..95
-          mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
-                 (it > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
-        // at d = 64 the previous dQ partial must have been read out of its columns
-        if (kOwnDQ && it > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(it - 1) & 1u, ctl, 112))) break;
-        tc_fence_after();
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            // dS^T of queries 0-63 in columns tDS + 0..31, of queries 64-127 in tDS + 64..95
+            mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
+                   (it > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
+          // at d = 64 the previous dQ partial must have been read out of its columns
+          if (kOwnDQ && g > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tQ, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
-        mma_commit(bar(L::bdQFull));
-        mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
-        if (!kOwnDQ && !(ok = issue_next_s(it))) break;
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ss(tQ, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
+          mma_commit(bar(L::bdQFull));
+          mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
+          if (!kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
+          i = inext;
+        }
+        if (ok) mma_commit(bar(L::bFinal));   // dV and dK of the item are complete
       }
-      mma_commit(bar(L::bFinal));
       mma_commit(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
@@ -302,163 +350,193 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const int cw = warp >> 2;
     const int cb = 64 * cw;
     const int r = tid & 127;
-    const int krow = kTile * kj + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int i = next_live(0);
-    for (int it = 0; it < len && ok; ++it, i = next_live(i + 1)) {
-      const bool partial = tile_state(i, kj, kvl, p.nT, p.causal, p.block_mask) == kPartial;
-      const int s = it % L::kStages;
-      if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(it / L::kStages) & 1u, ctl, 120))) break;
-      if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)it & 1u, ctl, 121))) break;
-      tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
-      const float* dlt = lse2 + kTile;
-      float x[64];
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tS + lane_off + (uint32_t)cb, u0);
-        tmem_ld32(tS + lane_off + (uint32_t)cb + 32u, u1);
-        tmem_ld_wait(u0);
-        tmem_ld_wait(u1);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(u0[c]);
-          x[32 + c] = __uint_as_float(u1[c]);
+    int g = 0, nf = 0;
+    int pending = -1;   // K/V buffer whose epilogue store has not been waited for yet (thread r == 0)
+    // the store out of buffer `pending` has read its staging: the buffer goes
+    // back to the producer
+    auto release_kv = [&]() {
+      if (pending >= 0) {
+        if (r == 0) {
+          bulk_wait_group_read_all();
+          mbar_arrive(bar(L::bKVFree + pending));
         }
+        pending = -1;
       }
-      // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
+    };
+    for (int k = 0; ok; ++k) {
+      const int item = item_index(k);
+      if (item >= total) break;
+      const Item w = item_at(item);
+      const int krow = kTile * w.kj + r;
+      int i = next_live(w, 0);
+      const bool live = i < p.nT;
+      for (int it = 0; i < p.nT; ++it, ++g, i = next_live(w, i + 1)) {
+        const bool partial = tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kPartial;
+        const int s = g % L::kStages;
+        if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 120))) break;
+        if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 121))) break;
+        tc_fence_after();
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
+        const float* dlt = lse2 + kTile;
+        float x[64];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tS + lane_off + (uint32_t)cb, u0);
+          tmem_ld32(tS + lane_off + (uint32_t)cb + 32u, u1);
+          tmem_ld_wait(u0);
+          tmem_ld_wait(u1);
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l = reinterpret_cast<const float4*>(lse2)[c4];   // one broadcast load per 4 queries
-        x[4 * c4] = ex2(fmaf(x[4 * c4], sl2, -l.x));
-        x[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], sl2, -l.y));
-        x[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], sl2, -l.z));
-        x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
-      }
-      if (partial) {
-        const int q0 = kTile * i + cb;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if ((p.causal && krow > q0 + c) || krow >= kvl) x[c] = 0.f;
-      }
-      // dropout: keep bits of this warpgroup's 64 query columns; one generator
-      // call (counter (query / 4, key / 4, bh, 0)) covers 4 queries, byte
-      // key mod 4 of each of its 4 words
-      uint32_t keep[2] = {0u, 0u};
-      if constexpr (DROP) {
-        const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
-        const uint32_t sh = 8u * ((uint32_t)krow & 3u);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const uint4 w = philox4x32_10(qb0 + (uint32_t)m, (uint32_t)krow >> 2, (uint32_t)bh, 0u,
-                                        p.drop.seed_lo, p.drop.seed_hi);
-          const uint32_t bits = (((w.x >> sh) & 0xFFu) >= p.drop.t ? 1u : 0u) |
-                                (((w.y >> sh) & 0xFFu) >= p.drop.t ? 2u : 0u) |
-                                (((w.z >> sh) & 0xFFu) >= p.drop.t ? 4u : 0u) |
-                                (((w.w >> sh) & 0xFFu) >= p.drop.t ? 8u : 0u);
-          keep[m >> 3] |= bits << (4 * (m & 7));
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(u0[c]);
+            x[32 + c] = __uint_as_float(u1[c]);
+          }
         }
-      }
-      auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
-      // the dV operand is the dropped P (P * Z * keep_scale), packed two
-      // queries per TMEM column into the first half of this warpgroup's own
-      // S columns (the other warpgroup may still be reading its half)
-      {
-        uint32_t pk[32];
+        // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int c0 = 2 * c;
-          if constexpr (DROP)
-            pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
-                               kept(c0 + 1) ? x[c0 + 1] * p.drop.keep_scale : 0.f);
-          else
-            pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = reinterpret_cast<const float4*>(lse2)[c4];   // one broadcast load per 4 queries
+          x[4 * c4] = ex2(fmaf(x[4 * c4], sl2, -l.x));
+          x[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], sl2, -l.y));
+          x[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], sl2, -l.z));
+          x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
         }
-        tmem_st32(tS + lane_off + (uint32_t)cb, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_warp(bar(L::bPFull));
+        if (partial) {
+          const int q0 = kTile * i + cb;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
+        }
+        // dropout: keep bits of this warpgroup's 64 query columns; one generator
+        // call (counter (query / 4, key / 4, bh, 0)) covers 4 queries, byte
+        // key mod 4 of each of its 4 words
+        uint32_t keep[2] = {0u, 0u};
+        if constexpr (DROP) {
+          const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
+          const uint32_t sh = 8u * ((uint32_t)krow & 3u);
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const uint4 v = philox4x32_10(qb0 + (uint32_t)m, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
+                                          p.drop.seed_lo, p.drop.seed_hi);
+            const uint32_t bits = (((v.x >> sh) & 0xFFu) >= p.drop.t ? 1u : 0u) |
+                                  (((v.y >> sh) & 0xFFu) >= p.drop.t ? 2u : 0u) |
+                                  (((v.z >> sh) & 0xFFu) >= p.drop.t ? 4u : 0u) |
+                                  (((v.w >> sh) & 0xFFu) >= p.drop.t ? 8u : 0u);
+            keep[m >> 3] |= bits << (4 * (m & 7));
+          }
+        }
+        auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
+        // the dV operand is the dropped P (P * Z * keep_scale), packed two
+        // queries per TMEM column into the first half of this warpgroup's own
+        // S columns (the other warpgroup may still be reading its half)
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int c0 = 2 * c;
+            if constexpr (DROP)
+              pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
+                                 kept(c0 + 1) ? x[c0 + 1] * p.drop.keep_scale : 0.f);
+            else
+              pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
+          }
+          tmem_st32(tS + lane_off + (uint32_t)cb, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::bPFull));
+        if (it == 0) release_kv();   // the previous item's store has had this tile's time to read its staging
 
-      // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> 16-bit -> swizzled smem
-      if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)it & 1u, ctl, 122))) break;
-      if (it > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(it - 1) & 1u, ctl, 123))) break;
-      tc_fence_after();
+        // dS^T row: ds[c] = p[c] * (dP[c] - D[query c]) -> 16-bit -> swizzled smem
+        if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)g & 1u, ctl, 122))) break;
+        if (g > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(g - 1) & 1u, ctl, 123))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, u);
+          tmem_ld_wait(u);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int c0 = 32 * cc + 2 * c;
+            float g0 = __uint_as_float(u[2 * c]), g1 = __uint_as_float(u[2 * c + 1]);
+            if constexpr (DROP) {   // dP = (dO V^T) * Z * keep_scale
+              g0 = kept(c0) ? g0 * p.drop.keep_scale : 0.f;
+              g1 = kept(c0 + 1) ? g1 * p.drop.keep_scale : 0.f;
+            }
+            const float2 dl = reinterpret_cast<const float2*>(dlt)[c0 >> 1];
+            const float d0 = x[c0] * (g0 - dl.x);
+            const float d1 = x[c0 + 1] * (g1 - dl.y);
+            pk[c] = pack2<F16>(d0, d1);
+          }
+          // dS^T also goes to TMEM (the A operand of dK), packed: at d = 128 into
+          // the second half of this warpgroup's S columns, after its P; at d = 64
+          // over this warpgroup's dP columns, which it has already read
+          tmem_st16(tDS + lane_off + (uint32_t)cb + 16u * cc, pk);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            uint8_t* dst = smem + L::kdS + swz_off(r, cb + 32 * cc + 8 * k4);
+            *reinterpret_cast<uint4*>(dst) =
+                make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::bdSFull));
+      }
+
+      // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK, for every key
+      // row of the tile (zeros when no query tile was live), staged in the
+      // item's V or K buffer once every MMA has read it, and stored by TMA
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      release_kv();   // the buffer of an earlier item without live query tiles
+      const int kb = k % L::kKV;
+      if (!(ok = mbar_wait_warp(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 124))) break;
+      if (live && !(ok = mbar_wait_warp(bar(L::bFinal), (uint32_t)nf & 1u, ctl, 125))) break;
+      nf += live ? 1 : 0;
+      tc_fence_after();
+      const uint32_t tacc = (cw == 0 ? tdV : tdK) + lane_off;
+      const float mul = (cw == 0) ? 1.f : scale;
+      const int stage_off = (cw == 0 ? L::kV : L::kK) + kb * L::kKVBytes;
+      uint8_t* stage = smem + stage_off;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t u[32];
-        tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, u);
-        tmem_ld_wait(u);
+        if (live) {
+          tmem_ld32(tacc + 32u * cc, u);
+          tmem_ld_wait(u);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) u[c] = 0u;
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int c0 = 32 * cc + 2 * c;
-          float g0 = __uint_as_float(u[2 * c]), g1 = __uint_as_float(u[2 * c + 1]);
-          if constexpr (DROP) {   // dP = (dO V^T) * Z * keep_scale
-            g0 = kept(c0) ? g0 * p.drop.keep_scale : 0.f;
-            g1 = kept(c0 + 1) ? g1 * p.drop.keep_scale : 0.f;
-          }
-          const float2 dl = reinterpret_cast<const float2*>(dlt)[c0 >> 1];
-          const float d0 = x[c0] * (g0 - dl.x);
-          const float d1 = x[c0 + 1] * (g1 - dl.y);
-          pk[c] = pack2<F16>(d0, d1);
-        }
-        // dS^T also goes to TMEM (the A operand of dK), packed: at d = 128 into
-        // the second half of this warpgroup's S columns, after its P; at d = 64
-        // over this warpgroup's dP columns, which it has already read
-        tmem_st16(tDS + lane_off + (uint32_t)cb + 16u * cc, pk);
+        for (int c = 0; c < 16; ++c)
+          pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint8_t* dst = smem + L::kdS + swz_off(r, cb + 32 * cc + 8 * k);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
         }
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive_warp(bar(L::bdSFull));
-    }
-
-    // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK, for every key
-    // row of the tile (zeros when no query tile was live), staged in the V or
-    // K buffer and stored by TMA
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    ok = ok && mbar_wait_warp(bar(L::bKV), 0, ctl, 124);
-    const bool have = ok && len > 0 && mbar_wait_warp(bar(L::bFinal), 0, ctl, 125);
-    tc_fence_after();
-    const uint32_t tacc = (cw == 0 ? tdV : tdK) + lane_off;
-    const float mul = (cw == 0) ? 1.f : scale;
-    uint8_t* stage = smem + (cw == 0 ? L::kV : L::kK);
-#pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-      uint32_t u[32];
-      if (have) {
-        tmem_ld32(tacc + 32u * cc, u);
-        tmem_ld_wait(u);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) u[c] = 0u;
+      fence_proxy_async_smem();
+      named_bar_sync(1 + cw, 128);
+      if (r == 0) {
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
+        bulk_commit_group();
       }
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-      }
+      pending = kb;
+      // with one K/V buffer the next item's K and V wait for this store
+      if (L::kKV == 1) release_kv();
     }
-    fence_proxy_async_smem();
-    named_bar_sync(1 + cw, 128);
-    if (r == 0) {
-      for (int h = 0; h < L::kHalves; ++h)
-        tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + (cw == 0 ? L::kV : L::kK) + h * 16384, 64 * h, kTile * kj, bh);
-      bulk_commit_group();
-      bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
-    }
+    if (r == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
@@ -472,55 +550,62 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const int r = tid - 256;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
-    int i = next_live(0);
-    for (int it = 0; it < len; ++it, i = next_live(i + 1)) {
-      const int s = it % L::kStages;
-      const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
-      if (!mbar_wait_warp(bar(L::bdQFull), (uint32_t)it & 1u, ctl, 130)) break;
-      tc_fence_after();
-      uint32_t u[kBoxesPerRound][32];
+    bool ok = true;
+    int g = 0;
+    for (int k = 0; ok; ++k) {
+      const int item = item_index(k);
+      if (item >= total) break;
+      const Item w = item_at(item);
+      for (int i = next_live(w, 0); i < p.nT; ++g, i = next_live(w, i + 1)) {
+        const int s = g % L::kStages;
+        const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
+        if (!(ok = mbar_wait_warp(bar(L::bdQFull), (uint32_t)g & 1u, ctl, 130))) break;
+        tc_fence_after();
+        uint32_t u[kBoxesPerRound][32];
 #pragma unroll
-      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld32(tQ + lane_off + 32u * b, u[b]);
+        for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld32(tQ + lane_off + 32u * b, u[b]);
 #pragma unroll
-      for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
+        for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
 #pragma unroll
-      for (int round = 0; round < kRounds; ++round) {
-        if (round == kRounds - 1) {
-          tc_fence_before();
-          mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
-        }
-        if (round > 0) {              // the previous round has been read out of the slot
-          if (r == 0) bulk_wait_group_read_all();
-          named_bar_sync(3, 128);
-        }
-#pragma unroll
-        for (int b = 0; b < kBoxesPerRound; ++b)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {    // 8 chunks of 4 fp32 per 32-column box
-            const uint32_t o = sw + (uint32_t)((k ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(smem + stage + 16384 * b + o) =
-                make_uint4(u[b][4 * k], u[b][4 * k + 1], u[b][4 * k + 2], u[b][4 * k + 3]);
+        for (int round = 0; round < kRounds; ++round) {
+          if (round == kRounds - 1) {
+            tc_fence_before();
+            mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
           }
-        fence_proxy_async_smem();
-        named_bar_sync(3, 128);
+          if (round > 0) {              // the previous round has been read out of the slot
+            if (r == 0) bulk_wait_group_read_all();
+            named_bar_sync(3, 128);
+          }
+#pragma unroll
+          for (int b = 0; b < kBoxesPerRound; ++b)
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {    // 8 chunks of 4 fp32 per 32-column box
+              const uint32_t o = sw + (uint32_t)((k8 ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(smem + stage + 16384 * b + o) =
+                  make_uint4(u[b][4 * k8], u[b][4 * k8 + 1], u[b][4 * k8 + 2], u[b][4 * k8 + 3]);
+            }
+          fence_proxy_async_smem();
+          named_bar_sync(3, 128);
+          if (r == 0) {
+#pragma unroll
+            for (int b = 0; b < kBoxesPerRound; ++b)
+              if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
+                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b),
+                                  kTile * i, w.bh);
+            bulk_commit_group();
+          }
+          if (round + 1 < kRounds) {    // the next columns into registers while the round is read
+#pragma unroll
+            for (int b = 0; b < kBoxesPerRound; ++b)
+              tmem_ld32(tQ + lane_off + 32u * ((round + 1) * kBoxesPerRound + b), u[b]);
+#pragma unroll
+            for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
+          }
+        }
         if (r == 0) {
-#pragma unroll
-          for (int b = 0; b < kBoxesPerRound; ++b)
-            if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
-              tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b), kTile * i, bh);
-          bulk_commit_group();
+          bulk_wait_group_read_all();
+          mbar_arrive(bar(L::bdOFree + s));
         }
-        if (round + 1 < kRounds) {    // the next columns into registers while the round is read
-#pragma unroll
-          for (int b = 0; b < kBoxesPerRound; ++b)
-            tmem_ld32(tQ + lane_off + 32u * ((round + 1) * kBoxesPerRound + b), u[b]);
-#pragma unroll
-          for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
-        }
-      }
-      if (r == 0) {
-        bulk_wait_group_read_all();
-        mbar_arrive(bar(L::bdOFree + s));
       }
     }
     if (r == 0) bulk_wait_group_all();     // reductions complete before exit
@@ -616,7 +701,14 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const dim3 grid((unsigned)(p.nT * p.B * p.H));
+  // persistent: at most one CTA per SM (the kernel holds all of TMEM), each
+  // looping over its share of the (key tile, batch-head) items
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = (long long)p.nT * p.B * p.H;
+  const dim3 grid((unsigned)(items < sms ? items : sms));
   fa_bwd_main_kernel<D, F16, DROP><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
   return cudaGetLastError();
 }
