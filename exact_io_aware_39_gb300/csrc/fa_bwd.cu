@@ -12,10 +12,16 @@
 // Three launches on one stream:
 //   1. fa_bwd_pre:  D = rowsum(dO * O) in fp32, LSE2 = LSE * log2(e) (+inf on
 //      rows past N and on fully masked rows), dQ accumulator zeroed;
-//   2. fa_bwd_main: one CTA per (batch, head, 128-key tile), looping over the
-//      live 128-query tiles. TMEM holds dV and dK (accumulated over the whole
-//      loop), S^T, then P^T as packed bf16 in place, and dP^T, which is then
-//      reused for the dQ partial of the tile. Five tcgen05 MMAs per tile pair:
+//   2. fa_bwd_main: persistent, one CTA per SM. A CTA walks its share of the
+//      (128-key tile, batch-head) items (key tiles with the most live query
+//      tiles first, alternating direction per round so that the shares
+//      balance) and, for each, loops over the live 128-query tiles. The Q/dO
+//      ring and every barrier phase run on across items; K and V are double
+//      buffered at d = 64, so that the next item's key tile loads while this
+//      one's dV and dK are stored through the other buffer. TMEM holds dV and
+//      dK (accumulated over the item's loop), S^T, then P^T as packed bf16 in
+//      place, and dP^T, which is then reused for the dQ partial of the tile.
+//      Five tcgen05 MMAs per tile pair:
 //        S^T  = K Q^T          (A = K, B = Q,   both K-major)
 //        dP^T = V dO^T         (A = V, B = dO,  both K-major)
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
