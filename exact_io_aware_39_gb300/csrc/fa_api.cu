@@ -282,13 +282,16 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
     return FA_ERR_CUDA;
   CUtensorMap tdq;
   if (make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
-  if (launch_bwd_pre(o.f16, O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
+  if (launch_bwd_pre(o.f16, O, dO, LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
+    return FA_ERR_CUDA;
   BwdParams p{};
   p.kv_len = kv_len;
   p.block_mask = block_mask;
   p.dq_acc = dq_acc;
   p.lse2 = lse2;
   p.delta = delta;
+  p.sched = sched;
   p.err = ds->err;
   p.B = B;
   p.H = H;

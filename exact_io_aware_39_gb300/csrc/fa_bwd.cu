@@ -12,10 +12,10 @@
 // Three launches on one stream:
 //   1. fa_bwd_pre:  D = rowsum(dO * O) in fp32, LSE2 = LSE * log2(e) (+inf on
 //      rows past N and on fully masked rows), dQ accumulator zeroed;
-//   2. fa_bwd_main: persistent, one CTA per SM. A CTA walks its share of the
-//      (128-key tile, batch-head) items (key tiles with the most live query
-//      tiles first, alternating direction per round so that the shares
-//      balance) and, for each, loops over the live 128-query tiles. The Q/dO
+//   2. fa_bwd_main: persistent, one CTA per SM. The (128-key tile,
+//      batch-head) items are handed out in order (key tiles with the most live
+//      query tiles first) from a grid-wide counter, each to the first CTA
+//      ready for one; a CTA loops over the live 128-query tiles of each. The Q/dO
 //      ring and every barrier phase run on across items; K and V are double
 //      buffered at d = 64, so that the next item's key tile loads while this
 //      one's dV and dK are stored through the other buffer. TMEM holds dV and
@@ -90,9 +90,14 @@ struct BwdLayout {
   static constexpr int bFinal = bdQFree + 1;
   static constexpr int bDrain = bFinal + 1;
   static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (2 arrivals)
-  static constexpr int kNumBars = bKVFree + kKV;
+  // work items reach the other roles through a ring filled by the producer
+  static constexpr int kItemRing = 4;
+  static constexpr int bItemFull = bKVFree + kKV;            // [kItemRing]
+  static constexpr int bItemEmpty = bItemFull + kItemRing;   // [kItemRing]: MMA thread + 8 compute + 4 drain warps
+  static constexpr int kNumBars = bItemEmpty + kItemRing;
   static constexpr int kMisc = kBar + 8 * kNumBars;
-  static constexpr int kSmemBytes = kMisc + 16;
+  static constexpr int kRing = kMisc + 16;                    // [kItemRing] item indices
+  static constexpr int kSmemBytes = kRing + 4 * kItemRing;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -120,16 +125,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   const int BH = p.B * p.H;
   const int Np = p.nT * kTile;
-  // Work items are (key tile, batch-head) pairs, L = kj * BH + bh, low key
-  // tiles (the most live query tiles) first. A CTA takes item
-  // k * gridDim.x + (its index, or the mirrored index on odd k): the rounds
-  // alternate direction so that the CTAs' shares of long and short items
-  // balance.
+  // Work items are (key tile, batch-head) pairs, item = kj * BH + bh, low key
+  // tiles (the most live query tiles) first. A CTA starts with item
+  // blockIdx.x and then takes the next unclaimed one from a grid-wide counter
+  // (zeroed by the pre-pass), so that items are handed out in order, each to
+  // the first CTA that is ready for one.
   const int total = p.nT * BH;
-  auto item_index = [&](int k) -> int {
-    const int pos = (k & 1) ? (int)(gridDim.x - 1u - blockIdx.x) : (int)blockIdx.x;
-    return k * (int)gridDim.x + pos;
-  };
   struct Item {
     int kj, bh, kvl;   // key tile, batch-head, key length of the batch entry
   };
@@ -150,6 +151,21 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     return i;
   };
   Ctl ctl{p.err, abort_flag};
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
+  // item k of this CTA from the ring; -1 when none is left or a wait failed
+  auto take_item = [&](int k, bool warp_wide, bool& ok) -> int {
+    const int rs = k % L::kItemRing;
+    const uint32_t ph = (uint32_t)(k / L::kItemRing) & 1u;
+    ok = warp_wide ? mbar_wait_warp(bar(L::bItemFull + rs), ph, ctl, 105)
+                   : mbar_wait(bar(L::bItemFull + rs), ph, ctl, 105);
+    if (!ok) return -1;
+    const int item = ring[rs];
+    if (warp_wide)
+      mbar_arrive_warp(bar(L::bItemEmpty + rs));
+    else
+      mbar_arrive(bar(L::bItemEmpty + rs));
+    return item;
+  };
 
   if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
     if (tid == 0) {
@@ -163,7 +179,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
       mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u
-                        : i == L::bdQFree ? 4u : i >= L::bKVFree ? 2u : 1u);   // arrivals
+                        : i == L::bdQFree ? 4u
+                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 2u
+                        : i >= L::bItemEmpty ? 13u : 1u);   // arrivals
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -223,7 +241,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       bool ok = true;
       int g = 0;
       for (int k = 0; ok; ++k) {
-        const int item = item_index(k);
+        // claim the next item and hand it to the other roles
+        const int rs = k % L::kItemRing;
+        if (k >= L::kItemRing &&
+            !(ok = mbar_wait(bar(L::bItemEmpty + rs), (uint32_t)(k / L::kItemRing - 1) & 1u, ctl, 104)))
+          break;
+        const int item = k == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(p.sched, 1u);
+        ring[rs] = item < total ? item : -1;
+        mbar_arrive(bar(L::bItemFull + rs));
         if (item >= total) break;
         const Item w = item_at(item);
         int i = next_live(w, 0);
@@ -287,8 +312,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int item = item_index(k);
-        if (item >= total) break;
+        const int item = take_item(k, false, ok);
+        if (item < 0) break;
         const Item w = item_at(item);
         int i = next_live(w, 0);
         if (i >= p.nT) continue;
@@ -373,8 +398,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
     };
     for (int k = 0; ok; ++k) {
-      const int item = item_index(k);
-      if (item >= total) break;
+      const int item = take_item(k, true, ok);
+      if (item < 0) break;
       const Item w = item_at(item);
       const int krow = kTile * w.kj + r;
       int i = next_live(w, 0);
@@ -559,8 +584,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     bool ok = true;
     int g = 0;
     for (int k = 0; ok; ++k) {
-      const int item = item_index(k);
-      if (item >= total) break;
+      const int item = take_item(k, true, ok);
+      if (item < 0) break;
       const Item w = item_at(item);
       for (int i = next_live(w, 0); i < p.nT; ++g, i = next_live(w, i + 1)) {
         const int s = g % L::kStages;
@@ -626,15 +651,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 }
 
 // D = rowsum(dO * O) (fp32), LSE2 = LSE * log2(e) with +inf for -inf and
-// padding rows, dQ accumulator zeroed. A group of G threads per row (G the
+// padding rows, dQ accumulator and the main kernel's work counter zeroed. A group of G threads per row (G the
 // power of two >= d / 8); thread `part` owns columns 8 part .. 8 part + 7 when
 // 8 part < d.
 template <int G, bool F16>
 __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                   const float* __restrict__ lse, float* __restrict__ dq_acc,
-                                  float* __restrict__ lse2, float* __restrict__ delta, int BH, int N, int Np,
-                                  int d) {
+                                  float* __restrict__ lse2, float* __restrict__ delta,
+                                  unsigned int* __restrict__ sched, int BH, int N, int Np, int d) {
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid == 0) *sched = 0u;
   const long long row = gid / G;           // over BH * Np
   const int part = (int)(gid % G);
   if (row >= (long long)BH * Np) return;   // whole groups leave together (G divides the block)
@@ -722,7 +748,7 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
 }  // namespace
 
 cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const float* lse, float* dq_acc, float* lse2,
-                           float* delta, int BH, int N, int nT, int d, cudaStream_t s) {
+                           float* delta, unsigned int* sched, int BH, int N, int nT, int d, cudaStream_t s) {
   const int Np = nT * kTile;
   int G = 1;
   while (G < d / 8) G <<= 1;              // 1 .. 16: divides the block and the warp
@@ -734,9 +760,9 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
 #define FA_PRE_CASE(GG)                                                                                     \
   if (G == GG) {                                                                                            \
     if (f16)                                                                                                \
-      fa_bwd_pre_kernel<GG, true><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, BH, N, Np, d);  \
+      fa_bwd_pre_kernel<GG, true><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d); \
     else                                                                                                    \
-      fa_bwd_pre_kernel<GG, false><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, BH, N, Np, d); \
+      fa_bwd_pre_kernel<GG, false><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d); \
     return cudaGetLastError();                                                                              \
   }
   FA_PRE_CASE(1)

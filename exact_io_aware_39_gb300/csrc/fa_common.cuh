@@ -67,6 +67,7 @@ struct BwdParams {
   float* dq_acc;              // [BH, nT*128, d] fp32 workspace
   const float* lse2;          // [BH, nT*128] fp32 workspace: LSE * log2(e), +inf on padding
   const float* delta;         // [BH, nT*128] fp32 workspace: rowsum(dO * O)
+  unsigned int* sched;        // workspace word: next work item of the persistent main kernel (zeroed by the pre-pass)
   unsigned int* err;
   int B, H, N, nT;
   int causal;
@@ -89,7 +90,7 @@ cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
 
 cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const float* lse, float* dq_acc,
-                           float* lse2, float* delta, int BH, int N, int nT, int d,
+                           float* lse2, float* delta, unsigned int* sched, int BH, int N, int nT, int d,
                            cudaStream_t s);
 
 // tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 128 x 1,
@@ -115,7 +116,7 @@ int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, in
 
 // Workspace layout of the backward pass (byte offsets, 256-aligned sections).
 struct BwdWorkspace {
-  size_t dq_off, lse2_off, delta_off, total;
+  size_t dq_off, lse2_off, delta_off, sched_off, total;
 };
 
 inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
@@ -126,7 +127,8 @@ inline BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   w.dq_off = 0;
   w.lse2_off = al(w.dq_off + BH * Np * d * sizeof(float));
   w.delta_off = al(w.lse2_off + BH * Np * sizeof(float));
-  w.total = al(w.delta_off + BH * Np * sizeof(float));
+  w.sched_off = al(w.delta_off + BH * Np * sizeof(float));   // work counter of the main kernel
+  w.total = w.sched_off + 256;
   return w;
 }
 

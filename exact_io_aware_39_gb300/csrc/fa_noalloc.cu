@@ -93,13 +93,16 @@ extern "C" fa_status flash_attn_bwd_noalloc(const void* Q, const void* K, const 
   CUtensorMap tdq;
   if (internal_make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
   // the pre-pass zeroes the dQ accumulator and rewrites both row vectors
-  if (launch_bwd_pre(false, O, dO, LSE, dq_acc, lse2, delta, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
+  if (launch_bwd_pre(false, O, dO, LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
+    return FA_ERR_CUDA;
   BwdParams p{};
   p.kv_len = kv_len;
   p.block_mask = block_mask;
   p.dq_acc = dq_acc;
   p.lse2 = lse2;
   p.delta = delta;
+  p.sched = sched;
   p.err = err;
   p.B = B;
   p.H = H;

@@ -118,8 +118,9 @@ fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O
 
 /*
  * Bytes of device workspace flash_attn_bwd needs for this shape (fp32 dQ
- * accumulator [B, H, nT*128, d] plus two fp32 row vectors [B, H, nT*128]).
- * Returns 0 for an invalid shape.
+ * accumulator [B, H, nT*128, d], two fp32 row vectors [B, H, nT*128] and a
+ * 256-byte block holding the work counter of the persistent kernel; each
+ * section 256-byte aligned). Returns 0 for an invalid shape.
  */
 size_t flash_attn_bwd_workspace_size(int B, int H, int N, int d);
 

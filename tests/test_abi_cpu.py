@@ -54,9 +54,10 @@ def test_workspace_size_formula(lib):
         return (x + 255) // 256 * 256
     for B, H, N, d in [(1, 2, 256, 64), (2, 3, 300, 128), (1, 32, 16384, 128)]:
         Np = (N + 127) // 128 * 128
-        want = al(al(B * H * Np * d * 4) + B * H * Np * 4) + al(B * H * Np * 4)
+        # dQ accumulator, LSE2 and D rows, then the 256-byte work-counter block
+        want = al(al(B * H * Np * d * 4) + B * H * Np * 4) + al(B * H * Np * 4) + 256
         assert L.flash_attn_bwd_workspace_size(B, H, N, d) == want
-    assert L.flash_attn_bwd_workspace_size(1, 1, 256, 96) == al(al(256 * 96 * 4) + 256 * 4) + al(256 * 4)
+    assert L.flash_attn_bwd_workspace_size(1, 1, 256, 96) == al(al(256 * 96 * 4) + 256 * 4) + al(256 * 4) + 256
     for bad_d in (0, 4, 60, 136, 256):
         assert L.flash_attn_bwd_workspace_size(1, 1, 256, bad_d) == 0
     assert L.flash_attn_bwd_workspace_size(0, 1, 256, 64) == 0

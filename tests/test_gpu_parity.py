@@ -134,6 +134,33 @@ def test_small_shapes_match_oracle(fa, spec):
     _compare(got, ref)
 
 
+# The backward kernel is persistent (one CTA per SM, each walking several
+# (key tile, batch-head) items with its pipeline running on across them):
+# shapes with more than twice as many key-tile items as SMs, including items
+# whose key tile has no live query tile (kv_len 0 and short lengths) and
+# block-sparse rows, compared in full.
+MANY_ITEMS = [
+    # name, B, N, d, causal, kv_len, block mask; H is chosen so that B * H * nT > 2.2 x SMs
+    ("many_items_kv_len_causal", 4, 512, 64, True, [512, 0, 300, 129], None),
+    ("many_items_d128_kv_len", 2, 384, 128, False, [384, 200], None),
+    ("many_items_block_mask", 2, 512, 64, False, None, "rand"),
+]
+
+
+@pytest.mark.parametrize("spec", MANY_ITEMS, ids=[s[0] for s in MANY_ITEMS])
+def test_many_items_per_cta_match_oracle(fa, spec):
+    name, B, N, d, causal, kv, bm = spec
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nT = (N + 127) // 128
+    H = max(2, math.ceil(2.2 * sms / (B * nT)))
+    assert B * H * nT > 2 * sms
+    c = _small_case(name, B, H, N, d, causal, kv, bm)
+    got = _run_gpu(fa, c)
+    ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], c["scale"], c["causal"],
+                                   c["kv_len"], c["block_mask"])
+    _compare(got, ref)
+
+
 # O bound of the head-dimension cases: 1e-2 plus the bf16 rounding of O itself
 # (8 significant bits: up to 2^-8 |O|), since rows that see only a few keys
 # (kv_len = 5) reach |O| > 2.5, where rounding alone approaches 1e-2.
