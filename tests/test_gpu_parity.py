@@ -329,6 +329,52 @@ def test_repeat_calls_are_deterministic_and_leave_guards(fa):
     assert fa.device_error()[0] == 0
 
 
+def test_concurrent_backward_calls_on_two_streams(fa):
+    """The persistent backward kernel hands out its work items from a counter
+    in the caller's workspace: two calls in flight at once on two streams,
+    each with its own workspace, give the bits of the same calls run one
+    after the other for dK and dV (each item is computed whole by one CTA)
+    and dQ within rounding (partials are added in arrival order)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = max(2, math.ceil(2.2 * sms / (2 * 4)))
+    cases = [_small_case("streams_a", 2, H, 512, 64, True, None, None),
+             _small_case("streams_b", 2, H, 512, 128, False, [512, 260], None)]
+    dev = torch.device("cuda:0")
+    prepared = []
+    for c in cases:
+        q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+        kv = None if c["kv_len"] is None else c["kv_len"].to(dev)
+        o, lse = fa.attention_fwd(q, k, v, c["scale"], c["causal"], kv, None)
+        prepared.append((c, q, k, v, do, kv, o, lse))
+
+    def run(args, stream, ws):
+        c, q, k, v, do, kv, o, lse = args
+        return fa.attention_bwd(q, k, v, o, do, lse, c["scale"], c["causal"], kv, None, workspace=ws,
+                                stream=stream)
+
+    workspaces = [torch.empty(fa.flash_attn_bwd_workspace_size(*a[1].shape), dtype=torch.uint8, device=dev)
+                  for a in prepared]
+    serial = [run(a, torch.cuda.current_stream(), ws) for a, ws in zip(prepared, workspaces)]
+    torch.cuda.synchronize()
+    serial = [[t.clone() for t in r] for r in serial]
+    streams = [torch.cuda.Stream(device=dev) for _ in prepared]
+    for s_ in streams:
+        s_.wait_stream(torch.cuda.current_stream())
+    together = []
+    for _ in range(3):
+        for a, ws, s_ in zip(prepared, workspaces, streams):
+            with torch.cuda.stream(s_):
+                together.append(run(a, s_, ws))
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    for rep in range(3):
+        for i in range(len(prepared)):
+            dq, dk, dv = together[2 * rep + i]
+            assert torch.equal(dk.view(torch.int16), serial[i][1].view(torch.int16))
+            assert torch.equal(dv.view(torch.int16), serial[i][2].view(torch.int16))
+            assert torch.allclose(dq.float(), serial[i][0].float(), rtol=1e-2, atol=1e-3)
+
+
 def test_invalid_arguments_on_device(fa):
     dev = torch.device("cuda:0")
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device=dev)
