@@ -43,6 +43,10 @@ CASES = [
     ("d128_block_mask", 1, 2, 640, 128, True, None, True, 0.2, 5, torch.bfloat16),
     ("fp16_d128", 1, 2, 384, 128, False, None, False, 0.3, 42, torch.float16),
     ("d80_causal", 1, 2, 300, 80, True, None, False, 0.2, 77, torch.bfloat16),
+    # more (key tile, batch-head) items than twice the SMs of a GB300 (152), so
+    # that the persistent backward kernel walks several items per CTA
+    ("d64_many_items_kv_len", 4, 21, 512, 64, True, [512, 0, 300, 129], False, 0.2, 11, torch.bfloat16),
+    ("d128_many_items", 2, 56, 384, 128, True, None, False, 0.1, 2**33 + 1, torch.bfloat16),
 ]
 
 
