@@ -726,18 +726,21 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                               const CUtensorMap& tdq, const BwdParams& p, float scale, cudaStream_t s) {
   using L = BwdLayout<D>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  // persistent: at most one CTA per SM (the kernel holds all of TMEM), each
-  // looping over its share of the (key tile, batch-head) items
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // the attribute belongs to each device's copy of the kernel
+  static bool configured[kMaxDevices] = {};
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  // persistent: at most one CTA per SM (the kernel holds all of TMEM), each
+  // taking (key tile, batch-head) items from the work counter
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));

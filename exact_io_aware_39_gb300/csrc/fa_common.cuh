@@ -11,6 +11,7 @@ namespace fa {
 
 constexpr int kTile = 128;            // rows of a Q tile and of a K/V tile
 constexpr int kMaxN = 131072;         // longest supported sequence
+constexpr int kMaxDevices = 64;       // device ordinals with per-device library state
 
 enum TileState : int { kSkip = 0, kFull = 1, kPartial = 2 };
 

@@ -473,12 +473,17 @@ template <int D, bool F16, bool DROP>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   using L = FwdLayout<D>;
-  static bool configured = false;   // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // the attribute belongs to each device's copy of the kernel
+  static bool configured[kMaxDevices] = {};
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));

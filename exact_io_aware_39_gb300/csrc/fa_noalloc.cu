@@ -37,7 +37,6 @@ constexpr size_t kScratchBytes = FA_BWD_NOALLOC_SCRATCH_BYTES;   // 64 MiB per d
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
