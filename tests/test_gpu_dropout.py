@@ -52,6 +52,7 @@ CASES = [
     # that the persistent backward kernel walks several items per CTA
     ("d64_many_items_kv_len", 4, 21, 512, 64, True, [512, 0, 300, 129], False, 0.2, 11, torch.bfloat16),
     ("d128_many_items", 2, 56, 384, 128, True, None, False, 0.1, 2**33 + 1, torch.bfloat16),
+    ("fp16_d64_many_items_kv_len", 4, 21, 512, 64, False, [512, 200, 0, 384], False, 0.15, 3, torch.float16),
 ]
 
 

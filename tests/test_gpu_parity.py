@@ -144,6 +144,7 @@ MANY_ITEMS = [
     ("many_items_kv_len_causal", 4, 512, 64, True, [512, 0, 300, 129], None),
     ("many_items_d128_kv_len", 2, 384, 128, False, [384, 200], None),
     ("many_items_block_mask", 2, 512, 64, False, None, "rand"),
+    ("many_items_d96_all_masks", 2, 640, 96, True, [600, 333], "rand"),
 ]
 
 
@@ -158,7 +159,7 @@ def test_many_items_per_cta_match_oracle(fa, spec):
     got = _run_gpu(fa, c)
     ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], c["scale"], c["causal"],
                                    c["kv_len"], c["block_mask"])
-    _compare(got, ref)
+    _compare(got, ref, o_rel=HEAD_DIM_O_REL if d not in (64, 128) else 0.0)
 
 
 # O bound of the head-dimension cases: 1e-2 plus the bf16 rounding of O itself
