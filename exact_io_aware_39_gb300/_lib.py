@@ -39,10 +39,14 @@ FA_DTYPE_BF16, FA_DTYPE_F16 = 0, 1
 class fa_options(ctypes.Structure):
     """Mirror of the C struct fa_options (size is set by the constructor)."""
     _fields_ = [("size", ctypes.c_uint32), ("dtype", ctypes.c_int32), ("p_drop", ctypes.c_float),
-                ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64)]
+                ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64),
+                ("tile_record", ctypes.c_void_p), ("wait_limit_us", ctypes.c_uint32),
+                ("test_stall", ctypes.c_uint32)]
 
-    def __init__(self, dtype=FA_DTYPE_BF16, p_drop=0.0, seed=0):
-        super().__init__(ctypes.sizeof(fa_options), dtype, float(p_drop), 0, int(seed))
+    def __init__(self, dtype=FA_DTYPE_BF16, p_drop=0.0, seed=0, tile_record=None, wait_limit_us=0,
+                 test_stall=0):
+        super().__init__(ctypes.sizeof(fa_options), dtype, float(p_drop), 0, int(seed), tile_record,
+                         int(wait_limit_us), int(test_stall))
 
 
 class FlashAttnError(RuntimeError):
@@ -223,13 +227,28 @@ def _mask_args(kv_len, block_mask):
     return _ptr(kv_len), _ptr(block_mask)
 
 
+def _set_checks(opts, tile_record, wait_limit_us, test_stall):
+    """Fills the checking fields of fa_options: tile_record (a zeroed CUDA
+    uint8 tensor [B, H, nT, nT] or None), wait_limit_us, test_stall."""
+    import torch
+    if tile_record is not None:
+        if tile_record.dtype != torch.uint8 or not tile_record.is_cuda or not tile_record.is_contiguous():
+            raise ValueError("tile_record must be a contiguous CUDA uint8 tensor [B, H, nT, nT]")
+        opts.tile_record = tile_record.data_ptr()
+    opts.wait_limit_us = int(wait_limit_us)
+    opts.test_stall = int(test_stall)
+
+
 def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, out=None, lse=None,
-                  stream=None, p_drop=0.0, seed=0):
+                  stream=None, p_drop=0.0, seed=0, tile_record=None, wait_limit_us=0, test_stall=0):
     """O, LSE = attention(q, k, v) on the GPU. q, k, v: bf16 or fp16 [B, H, N, d];
-    p_drop > 0 applies dropout to P (mask from Philox4x32-10 keyed by seed)."""
+    p_drop > 0 applies dropout to P (mask from Philox4x32-10 keyed by seed).
+    tile_record, wait_limit_us and test_stall are the checking options of
+    fa_options (see include/flash_attn.h)."""
     import torch
     opts = _check_inputs(q, k, v)
     opts.p_drop, opts.seed = float(p_drop), int(seed)
+    _set_checks(opts, tile_record, wait_limit_us, test_stall)
     B, H, N, d = q.shape
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -241,12 +260,14 @@ def attention_fwd(q, k, v, scale, causal=False, kv_len=None, block_mask=None, ou
 
 
 def attention_bwd(q, k, v, o, do, lse, scale, causal=False, kv_len=None, block_mask=None,
-                  workspace=None, dq=None, dk=None, dv=None, stream=None, p_drop=0.0, seed=0):
+                  workspace=None, dq=None, dk=None, dv=None, stream=None, p_drop=0.0, seed=0,
+                  tile_record=None, wait_limit_us=0, test_stall=0):
     """dQ, dK, dV of attention on the GPU (recomputing S, P and the dropout
     mask on chip); p_drop and seed must match the forward call."""
     import torch
     opts = _check_inputs(q, k, v, o, do)
     opts.p_drop, opts.seed = float(p_drop), int(seed)
+    _set_checks(opts, tile_record, wait_limit_us, test_stall)
     B, H, N, d = q.shape
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk

@@ -82,12 +82,14 @@ fa_status device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D view [BH, N, d] of a bf16 (or fp16) tensor, box 64 x 128 x 1, 128-byte
-// swizzle; rows past N read as zeros and are not written by stores.
-fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool f16 = false) {
+// 3-D view [BH, N, d] of a bf16 (or fp16) tensor, box 64 x rows x 1, 128-byte
+// swizzle; rows past N read as zeros and are not written by stores. Loads use
+// 128-row boxes (a whole tile); the outputs are stored by each warp for its
+// own 32 rows.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool f16, int rows = kTile) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box, estr,
@@ -96,12 +98,13 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D view [BH, Np, d] of the fp32 dQ accumulator, box 32 x 128 x 1 (one
-// 128-byte row per box row), 128-byte swizzle.
+// 3-D view [BH, Np, d] of the fp32 dQ accumulator, box 32 x 32 x 1 (one
+// 128-byte row per box row; each warp adds its own 32 query rows), 128-byte
+// swizzle.
 fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Np, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)Np * d * 4};
-  cuuint32_t box[3] = {32, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -112,6 +115,7 @@ fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) 
 struct Options {
   bool f16 = false;
   DropoutParams drop{0u, 0u, 0u, 1.0f};
+  CheckParams chk{nullptr, 2000000000ull, 0u};
 };
 
 // Reads the caller's options (NULL = defaults). Fields beyond the caller's
@@ -131,6 +135,13 @@ fa_status read_options(const fa_options* opt, Options* out) {
     out->drop.keep_scale = (float)(256.0 / (256.0 - (double)t));
     out->drop.seed_lo = (uint32_t)(opt->seed & 0xFFFFFFFFull);
     out->drop.seed_hi = (uint32_t)(opt->seed >> 32);
+  }
+  if (opt->size >= offsetof(fa_options, tile_record) + sizeof(uint8_t*)) out->chk.rec = opt->tile_record;
+  if (opt->size >= offsetof(fa_options, wait_limit_us) + sizeof(uint32_t) && opt->wait_limit_us != 0u)
+    out->chk.wait_ns = 1000ull * opt->wait_limit_us;
+  if (opt->size >= offsetof(fa_options, test_stall) + sizeof(uint32_t)) {
+    if (opt->test_stall > 1u) return FA_ERR_INVALID_ARG;
+    out->chk.stall = opt->test_stall;
   }
   return FA_OK;
 }
@@ -171,22 +182,79 @@ int internal_device_error_word(unsigned int** err) {
   return st;
 }
 
-int internal_read_options(const void* options, bool* f16, bool* dropout) {
+int internal_read_options(const void* options, bool* f16, bool* flash_only) {
   Options o;
   const fa_status st = read_options(static_cast<const fa_options*>(options), &o);
   if (st == FA_OK) {
     *f16 = o.f16;
-    *dropout = o.drop.t != 0u;
+    *flash_only = o.drop.t != 0u || o.chk.rec != nullptr || o.chk.stall != 0u;
   }
   return st;
 }
 
-int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
-  return make_map(m, base, BH, N, d);
+int internal_bwd_validate(const BwdArgs& a, const void* options) {
+  fa_status st = check_shape(a.B, a.H, a.N, a.d, a.scale, a.causal);
+  if (st != FA_OK) return st;
+  Options o;
+  if ((st = read_options(static_cast<const fa_options*>(options), &o)) != FA_OK) return st;
+  const void* ptrs[] = {a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
 }
 
-int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, int d) {
-  return make_dq_map(m, dq_acc, BH, Np, d);
+// The backward launch sequence over a workspace of at least
+// bwd_workspace_layout(...).total bytes (256-byte aligned): the pre-pass
+// (row statistics, zeroed dQ accumulator and work counter), the main kernel
+// (with the caller's profile events around it) and the dQ conversion.
+int internal_bwd_run(const BwdArgs& a, const void* options, void* workspace, void* stream) {
+  Options o;
+  fa_status st = read_options(static_cast<const fa_options*>(options), &o);
+  if (st != FA_OK) return st;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FA_OK) return st;
+  const int B = a.B, H = a.H, N = a.N, d = a.d;
+  const BwdWorkspace w = bwd_workspace_layout(B, H, N, d);
+  const int BH = B * H;
+  const int nT = (N + kTile - 1) / kTile;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  float* delta = reinterpret_cast<float*>(ws + w.delta_off);
+  unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  if (make_map(&tq, a.Q, BH, N, d, o.f16) || make_map(&tk, a.K, BH, N, d, o.f16) ||
+      make_map(&tv, a.V, BH, N, d, o.f16) || make_map(&tdo, a.dO, BH, N, d, o.f16) ||
+      make_map(&tdk, a.dK, BH, N, d, o.f16, 32) || make_map(&tdv, a.dV, BH, N, d, o.f16, 32) ||
+      make_dq_map(&tdq, dq_acc, BH, nT * kTile, d))
+    return FA_ERR_CUDA;
+  if (launch_bwd_pre(o.f16, a.O, a.dO, a.LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  BwdParams p{};
+  p.kv_len = a.kv_len;
+  p.block_mask = a.block_mask;
+  p.dq_acc = dq_acc;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.sched = sched;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.nT = nT;
+  p.causal = a.causal;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.drop = o.drop;
+  p.chk = o.chk;
+  p.d = d;
+  const ProfileScope prof(s);
+  prof.before();
+  const cudaError_t e = launch_bwd_main(d, o.f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
+  prof.after();
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_dq(o.f16, dq_acc, a.dQ, a.scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_len, const uint8_t* block_mask,
@@ -218,7 +286,7 @@ fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O
   const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
   if (make_map(&tq, Q, BH, N, d, o.f16) || make_map(&tk, K, BH, N, d, o.f16) ||
-      make_map(&tv, V, BH, N, d, o.f16) || make_map(&to, O, BH, N, d, o.f16))
+      make_map(&tv, V, BH, N, d, o.f16) || make_map(&to, O, BH, N, d, o.f16, 32))
     return FA_ERR_CUDA;
   FwdParams p{};
   p.lse = LSE;
@@ -232,6 +300,8 @@ fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.drop = o.drop;
+  p.chk = o.chk;
+  p.d = d;
   const ProfileScope prof(static_cast<cudaStream_t>(stream));
   prof.before();
   const cudaError_t e = launch_fwd(d, o.f16, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
@@ -254,58 +324,13 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
                             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                             float scale, int causal, const int32_t* kv_len, const uint8_t* block_mask,
                             const fa_options* options, void* workspace, size_t workspace_bytes, void* stream) {
-  fa_status st = check_shape(B, H, N, d, scale, causal);
+  const BwdArgs a{Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, kv_len, block_mask};
+  fa_status st = static_cast<fa_status>(internal_bwd_validate(a, options));
   if (st != FA_OK) return st;
-  Options o;
-  if ((st = read_options(options, &o)) != FA_OK) return st;
-  const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
-  for (const void* q : ptrs)
-    if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
   const BwdWorkspace w = bwd_workspace_layout(B, H, N, d);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
-  DeviceState* ds = nullptr;
-  if ((st = device_state(&ds)) != FA_OK) return st;
-  const int BH = B * H;
-  const int nT = (N + kTile - 1) / kTile;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
-  float* delta = reinterpret_cast<float*>(ws + w.delta_off);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (make_map(&tq, Q, BH, N, d, o.f16) || make_map(&tk, K, BH, N, d, o.f16) ||
-      make_map(&tv, V, BH, N, d, o.f16) || make_map(&tdo, dO, BH, N, d, o.f16) ||
-      make_map(&tdk, dK, BH, N, d, o.f16) || make_map(&tdv, dV, BH, N, d, o.f16))
-    return FA_ERR_CUDA;
-  CUtensorMap tdq;
-  if (make_dq_map(&tdq, dq_acc, BH, nT * kTile, d)) return FA_ERR_CUDA;
-  unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
-  if (launch_bwd_pre(o.f16, O, dO, LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
-    return FA_ERR_CUDA;
-  BwdParams p{};
-  p.kv_len = kv_len;
-  p.block_mask = block_mask;
-  p.dq_acc = dq_acc;
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.sched = sched;
-  p.err = ds->err;
-  p.B = B;
-  p.H = H;
-  p.N = N;
-  p.nT = nT;
-  p.causal = causal;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.drop = o.drop;
-  p.d = d;
-  const ProfileScope prof(s);
-  prof.before();
-  const cudaError_t e = launch_bwd_main(d, o.f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
-  prof.after();
-  if (e != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_bwd_dq(o.f16, dq_acc, dQ, scale, BH, N, nT, d, s) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  return static_cast<fa_status>(internal_bwd_run(a, options, workspace, stream));
 }
 
 fa_status flash_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,

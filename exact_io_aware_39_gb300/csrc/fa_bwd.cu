@@ -79,7 +79,7 @@ struct BwdLayout {
   static constexpr int bQFull = bKV + kKV;
   static constexpr int bQEmpty = bQFull + kStages;
   static constexpr int bdOFull = bQEmpty + kStages;        // [stages]
-  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA
+  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA (4 arrivals)
   static constexpr int bSFull = bdOFree + kStages;
   static constexpr int bPFull = bSFull + 1;
   static constexpr int bdPFull = bPFull + 1;
@@ -89,7 +89,7 @@ struct BwdLayout {
   static constexpr int bdQFree = bdQFull + 1;
   static constexpr int bFinal = bdQFree + 1;
   static constexpr int bDrain = bFinal + 1;
-  static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (2 arrivals)
+  static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (8 arrivals)
   // work items reach the other roles through a ring filled by the producer
   static constexpr int kItemRing = 4;
   static constexpr int bItemFull = bKVFree + kKV;            // [kItemRing]
@@ -125,19 +125,19 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   const int BH = p.B * p.H;
   const int Np = p.nT * kTile;
-  // Work items are (key tile, batch-head) pairs, item = kj * BH + bh, low key
-  // tiles (the most live query tiles) first. A CTA starts with item
-  // blockIdx.x and then takes the next unclaimed one from a grid-wide counter
-  // (zeroed by the pre-pass), so that items are handed out in order, each to
-  // the first CTA that is ready for one.
+  // Work items are (key tile, batch-head) pairs, ordered group by group of
+  // p.group heads (whose Q, dO and dQ accumulator fit in L2 together) and,
+  // within a group, low key tiles (the most live query tiles) first. A CTA
+  // starts with item blockIdx.x and then takes the next unclaimed one from a
+  // grid-wide counter (zeroed by the pre-pass), so that items are handed out
+  // in order, each to the first CTA that is ready for one.
   const int total = p.nT * BH;
   struct Item {
     int kj, bh, kvl;   // key tile, batch-head, key length of the batch entry
   };
   auto item_at = [&](int item) -> Item {
     Item w;
-    w.kj = item / BH;
-    w.bh = item % BH;
+    w.kj = split_grouped(item, p.group, p.nT, BH, &w.bh);
     w.kvl = effective_kv_len(p.kv_len, w.bh / p.H, p.N);
     return w;
   };
@@ -150,7 +150,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     while (i < p.nT && tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kSkip) ++i;
     return i;
   };
-  Ctl ctl{p.err, abort_flag};
+  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // item k of this CTA from the ring; -1 when none is left or a wait failed
   auto take_item = [&](int k, bool warp_wide, bool& ok) -> int {
@@ -170,7 +170,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
     if (tid == 0) {
       uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy};
+      Ctl c0{p.err, &dummy, p.chk.wait_ns};
       report_error(c0, kErrSmemAlign, 100);
     }
     return;
@@ -180,7 +180,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     for (int i = 0; i < L::kNumBars; ++i)
       mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u
                         : i == L::bdQFree ? 4u
-                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 2u
+                        : (i >= L::bdOFree && i < L::bdOFree + L::kStages) ? 4u     // the four drain warps
+                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 8u         // the eight compute warps
                         : i >= L::bItemEmpty ? 13u : 1u);   // arrivals
     *abort_flag = 0u;
     fence_mbar_init();
@@ -257,6 +258,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           continue;
         }
         for (int it = 0; i < p.nT; ++it, ++g, i = next_live(w, i + 1)) {
+          if (p.chk.stall != 0u && g >= 1) { ok = false; break; }   // test of the timeout path: Q of tile 1 never comes
           const int s = g % L::kStages;
           const uint32_t n = (uint32_t)(g / L::kStages);
           // Q and the row statistics once dK has read the slot's Q; dO once the
@@ -385,12 +387,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const float sl2 = p.scale_log2;
     bool ok = true;
     int g = 0, nf = 0;
-    int pending = -1;   // K/V buffer whose epilogue store has not been waited for yet (thread r == 0)
-    // the store out of buffer `pending` has read its staging: the buffer goes
-    // back to the producer
+    int pending = -1;   // K/V buffer whose epilogue stores have not been waited for yet
+    // the stores out of buffer `pending` have read its staging (each warp
+    // waits for its own): the buffer goes back to the producer
     auto release_kv = [&]() {
       if (pending >= 0) {
-        if (r == 0) {
+        if (lane == 0) {
           bulk_wait_group_read_all();
           mbar_arrive(bar(L::bKVFree + pending));
         }
@@ -410,6 +412,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 120))) break;
         if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 121))) break;
         tc_fence_after();
+        if (p.chk.rec != nullptr && tid == 0) {   // the tile as this kernel computes it
+          uint8_t* rc = p.chk.rec + ((size_t)w.bh * p.nT + i) * p.nT + w.kj;
+          *rc = (uint8_t)(*rc + (partial ? 2 : 1));
+        }
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
         const float* dlt = lse2 + kTile;
         float x[64];
@@ -555,26 +561,33 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
         }
       }
+      // each warp stores its own 32 key rows (boxes of 32 rows), so that no
+      // warp ever waits for another at a group-wide barrier
       tc_fence_before();
       fence_proxy_async_smem();
-      named_bar_sync(1 + cw, 128);
-      if (r == 0) {
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = kTile * w.kj + 32 * (warp & 3);
+        if (row0 < p.N)
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384 + 4096 * (warp & 3), 64 * h, row0,
+                         w.bh);
         bulk_commit_group();
       }
       pending = kb;
       // with one K/V buffer the next item's K and V wait for this store
       if (L::kKV == 1) release_kv();
     }
-    if (r == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
+    if (lane == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
-    // has completed) in two rounds of boxes of [128 rows x 32 fp32], 128-byte
-    // swizzled -> TMA reduce-add into the accumulator. The TMEM columns are
-    // released as soon as they are all in registers or staged; the slot goes
-    // back to the producer when the last round has been read.
+    // has completed) in two rounds of 32-column boxes, 128-byte swizzled ->
+    // TMA reduce-add into the accumulator; each warp adds its own 32 query
+    // rows (boxes of 32 rows x 32 fp32) and synchronises only within itself.
+    // The TMEM columns are released as soon as they are all in registers or
+    // staged; the slot goes back to the producer when all four warps' last
+    // round has been read.
     regs_dec<kDrainRegs>();
     constexpr int kBoxesPerRound = L::kTileBytes / 16384;    // 1 (d = 64) or 2 (d = 128)
     constexpr int kRounds = D / 32 / kBoxesPerRound;
@@ -603,9 +616,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tc_fence_before();
             mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
           }
-          if (round > 0) {              // the previous round has been read out of the slot
-            if (r == 0) bulk_wait_group_read_all();
-            named_bar_sync(3, 128);
+          if (round > 0) {              // this warp's previous round has been read out of the slot
+            if (lane == 0) bulk_wait_group_read_all();
+            __syncwarp();
           }
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b)
@@ -616,13 +629,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                   make_uint4(u[b][4 * k8], u[b][4 * k8 + 1], u[b][4 * k8 + 2], u[b][4 * k8 + 3]);
             }
           fence_proxy_async_smem();
-          named_bar_sync(3, 128);
-          if (r == 0) {
+          __syncwarp();
+          if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < kBoxesPerRound; ++b)
               if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
-                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b),
-                                  kTile * i, w.bh);
+                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b + 4096u * (uint32_t)(warp & 3),
+                                  32 * (round * kBoxesPerRound + b), kTile * i + 32 * (warp & 3), w.bh);
             bulk_commit_group();
           }
           if (round + 1 < kRounds) {    // the next columns into registers while the round is read
@@ -633,13 +646,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
           }
         }
-        if (r == 0) {
+        if (lane == 0) {
           bulk_wait_group_read_all();
           mbar_arrive(bar(L::bdOFree + s));
         }
       }
     }
-    if (r == 0) bulk_wait_group_all();     // reductions complete before exit
+    if (lane == 0) bulk_wait_group_all();     // reductions complete before exit
   }
 
   tc_fence_before();
@@ -729,22 +742,23 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  // the attribute belongs to each device's copy of the kernel
-  static bool configured[kMaxDevices] = {};
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  static PerDeviceOnce smem_set;
+  e = once_per_device(smem_set, dev, [] {
+    return cudaFuncSetAttribute(fa_bwd_main_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
+  BwdParams q = p;
+  // a head's Q and dO (16-bit) and its fp32 dQ accumulator are re-read by
+  // all of its key-tile items
+  q.group = l2_head_group(8.0 * p.N * p.d, p.B * p.H);
   // persistent: at most one CTA per SM (the kernel holds all of TMEM), each
   // taking (key tile, batch-head) items from the work counter
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
-  fa_bwd_main_kernel<D, F16, DROP><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale);
+  fa_bwd_main_kernel<D, F16, DROP><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
   return cudaGetLastError();
 }
 

@@ -2,8 +2,10 @@
 // classifier, kernel parameter blocks and the internal launcher interface.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,6 +53,19 @@ struct DropoutParams {
   float keep_scale;
 };
 
+// Run-time checks shared by the kernels. rec, when not null, is the caller's
+// uint8 [BH, nT, nT] record of the tiles a kernel computed: the thread that
+// decides whether a tile needs element masking adds 1 (no masking) or 2
+// (masking) to the tile's byte, so that a tile computed twice would show as a
+// larger value. wait_ns bounds every mbarrier wait. stall (test only, 0 in
+// normal use) makes a producer stop loading after its first tile, so that a
+// consumer's bounded wait runs out and the kernel reports a timeout.
+struct CheckParams {
+  uint8_t* rec;
+  unsigned long long wait_ns;
+  uint32_t stall;
+};
+
 struct FwdParams {
   float* lse;                 // [BH, N] fp32
   const int32_t* kv_len;      // [B] or null
@@ -60,6 +75,9 @@ struct FwdParams {
   int causal;
   float scale_log2;           // scale * log2(e)
   DropoutParams drop;
+  CheckParams chk;
+  int d;                      // head dimension of the tensors (<= the kernel's tile width)
+  int group;                  // heads per group of the CTA order (set by the launcher)
 };
 
 struct BwdParams {
@@ -74,15 +92,65 @@ struct BwdParams {
   int causal;
   float scale_log2;
   DropoutParams drop;
+  CheckParams chk;
   int d;                      // head dimension of the tensors (<= the kernel's tile width)
+  int group;                  // heads per group of the work-item order (set by the launcher)
 };
+
+// Heads per group when the work of a launch is ordered group by group so that
+// the data one group touches stays in L2 (~126 MB): bytes_per_head is what a
+// head keeps re-reading while its items run; groups get a 32 MB share, since
+// the items in flight can span two neighbouring groups and the rest of L2
+// holds streamed data.
+inline int l2_head_group(double bytes_per_head, int BH) {
+  const double budget = 32.0 * 1024 * 1024;
+  int g = (int)(budget / (bytes_per_head > 1.0 ? bytes_per_head : 1.0));
+  return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
+// Splits a work index of an order that walks groups of `group` heads, within
+// a group `inner` steps (inner-major) over the group's heads (the last group
+// may have fewer heads): returns the inner step and sets bh.
+__host__ __device__ __forceinline__ int split_grouped(int index, int group, int inner, int BH, int* bh) {
+  const int full = BH / group;              // groups of `group` heads
+  const int per = inner * group;
+  const int gi = index / per;
+  if (gi < full) {
+    const int rem = index - gi * per;
+    *bh = gi * group + rem % group;
+    return rem / group;
+  }
+  const int last = BH - full * group;       // heads of the last, smaller group
+  const int rem = index - full * per;
+  *bh = full * group + rem % last;
+  return rem / last;
+}
+
+// Calls f() once per device for a setting that belongs to each device's copy
+// of a kernel (its shared-memory limit); safe under concurrent callers.
+struct PerDeviceOnce {
+  std::atomic<bool> done[kMaxDevices];
+  std::mutex mu;
+};
+
+template <typename F>
+cudaError_t once_per_device(PerDeviceOnce& o, int dev, F&& f) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(o.mu);
+  if (o.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = f();
+  if (e == cudaSuccess) o.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // Head dimension of the kernel that serves a head dimension d (a multiple of
 // 8 up to 128): tiles are 64 or 128 columns wide; columns past d are zeros on
 // load (TMA out-of-bounds fill) and are not written on store.
 __host__ __device__ __forceinline__ int kernel_head_dim(int d) { return d <= 64 ? 64 : 128; }
 
-// Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1,
+// Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1
+// for loads and 64 x 32 x 1 for the stores of O, dK and dV (one box per warp),
 // 128-byte swizzle. d is the tensors' head dimension; the kernel instance is
 // chosen by kernel_head_dim(d). Return the cudaError_t of the launch.
 // f16 selects fp16 elements (else bf16) for Q, K, V, O, dO, dQ, dK, dV.
@@ -94,9 +162,9 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
                            float* lse2, float* delta, unsigned int* sched, int BH, int N, int nT, int d,
                            cudaStream_t s);
 
-// tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 128 x 1,
-// 128-byte swizzle (internal_make_dq_map); partial dQ tiles are added into it
-// with TMA reduce-add.
+// tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 32 x 1,
+// 128-byte swizzle; partial dQ tiles are added into it with TMA reduce-add,
+// each warp its own 32 query rows.
 cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tdq,
@@ -111,9 +179,27 @@ cudaError_t launch_tile_map(int B, int N, int nT, int causal, const int32_t* kv_
 // Host helpers defined with the C ABI (return fa_status values).
 int internal_check_shape(int B, int H, int N, int d, float scale, int causal);
 int internal_device_error_word(unsigned int** err);   // current device; runs its set-up once
-int internal_read_options(const void* options, bool* f16, bool* dropout);   // options: const fa_options*
-int internal_make_map(CUtensorMap* m, const void* base, int BH, int N, int d);   // bf16
-int internal_make_dq_map(CUtensorMap* m, const float* dq_acc, int BH, int Np, int d);
+// options: const fa_options* or null. flash_only: an option only the flash
+// kernels implement is set (dropout, tile record, test stall).
+int internal_read_options(const void* options, bool* f16, bool* flash_only);
+
+// Arguments of a backward call (the flash_attn_bwd signature without the
+// workspace and the stream).
+struct BwdArgs {
+  const void *Q, *K, *V, *O, *dO;
+  const float* LSE;
+  void *dQ, *dK, *dV;
+  int B, H, N, d;
+  float scale;
+  int causal;
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+};
+// Shape, pointer and option checks of a backward call (nothing launched).
+int internal_bwd_validate(const BwdArgs& a, const void* options);
+// The backward launch sequence over a validated call and a workspace of
+// bwd_workspace_layout(...).total bytes, 256-byte aligned.
+int internal_bwd_run(const BwdArgs& a, const void* options, void* workspace, void* stream);
 
 // Workspace layout of the backward pass (byte offsets, 256-aligned sections).
 struct BwdWorkspace {

@@ -96,9 +96,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   const int BH = p.B * p.H;
   const int nC = (p.nT + 1) >> 1;
-  const int L_ = blockIdx.x;
-  const int c = nC - 1 - L_ / BH;        // heaviest Q-tile pairs first
-  const int bh = L_ % BH;
+  // CTAs walk groups of p.group heads whose K and V fit in L2 together;
+  // within a group the heaviest Q-tile pairs come first
+  int bh = 0;
+  const int c = nC - 1 - split_grouped((int)blockIdx.x, p.group, nC, BH, &bh);
   const int b = bh / p.H;
   const int kvl = effective_kv_len(p.kv_len, b, p.N);
   const int qi0 = 2 * c;
@@ -108,12 +109,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
-  Ctl ctl{p.err, abort_flag};
+  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
 
   if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
     if (tid == 0) {
       uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy};
+      Ctl c0{p.err, &dummy, p.chk.wait_ns};
       report_error(c0, kErrSmemAlign, 0);
     }
     return;
@@ -169,6 +170,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                       kTile * (qi0 + t), bh);
       int nk = 0;   // K loads issued
       for (int e = 0; e < len; ++e) {
+        if (p.chk.stall != 0u && e >= 1) break;   // test of the timeout path: K of entry 1 never comes
         const int j = entry_j(list[e]);
         const int sk = e % L::kStagesK;
         const uint32_t nk_ = (uint32_t)(e / L::kStagesK);
@@ -307,6 +309,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       if (!entry_live(ent, t)) continue;
       if (!mbar_wait_warp(bar(L::bSFull + t), n & 1u, ctl, 10 + t)) { ok = false; break; }
       tc_fence_after();
+      if (p.chk.rec != nullptr && r == 0) {   // the tile as this kernel computes it
+        uint8_t* rc = p.chk.rec + ((size_t)bh * p.nT + qi) * p.nT + entry_j(ent);
+        *rc = (uint8_t)(*rc + (entry_partial(ent, t) ? 2 : 1));
+      }
       float x[128];
       {
         uint32_t u0[32], u1[32], u2[32], u3[32];
@@ -417,6 +423,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (ok) ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 12 + t);
       if (ok && n > 0) ok = mbar_wait_warp(bar(L::bOFinal + t), 0, ctl, 14 + t);
+      if (!ok) drain_wait(bar(L::bQFull), 0);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
       tc_fence_after();
       uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
       const float inv_l = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
@@ -450,11 +457,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         if (have_o && l > 0.f) lse = (m_ref + log2f(l)) * 0.69314718055994531f;
         p.lse[(size_t)bh * p.N + row] = lse;
       }
+      // each warp stores its own 32 rows (boxes of 32 rows), so that no warp
+      // ever waits for another at a group-wide barrier
       fence_proxy_async_smem();
-      named_bar_sync(1 + t, 128);
-      if (r == 0) {
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_store_3d(&to, smem_u32(stage) + h * 16384, 64 * h, kTile * qi, bh);
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = kTile * qi + 32 * (warp & 3);
+        if (row0 < p.N)
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_store_3d(&to, smem_u32(stage) + h * 16384 + 4096 * (warp & 3), 64 * h, row0, bh);
         bulk_commit_group();
         bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
       }
@@ -476,18 +487,18 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  // the attribute belongs to each device's copy of the kernel
-  static bool configured[kMaxDevices] = {};
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(fa_fwd_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  static PerDeviceOnce smem_set;
+  e = once_per_device(smem_set, dev, [] {
+    return cudaFuncSetAttribute(fa_fwd_kernel<D, F16, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
+  FwdParams q = p;
+  // a head's K and V (2 N d 16-bit elements) are re-read by all of its CTAs
+  q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));
-  fa_fwd_kernel<D, F16, DROP><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, p);
+  fa_fwd_kernel<D, F16, DROP><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, q);
   return cudaGetLastError();
 }
 

@@ -19,11 +19,12 @@ namespace fa {
 // error reporting
 // ---------------------------------------------------------------------------
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: default bound of a wait, and of every drain wait
 
 struct Ctl {
   unsigned int* err;          // global error word (4 x u32)
   volatile uint32_t* abort;   // shared abort flag of this CTA
+  uint64_t limit;             // bound of one mbarrier wait, ns
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -118,7 +119,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const C
     if (mbar_try(bar, parity)) return true;
     if ((++n & 15u) == 0u) {
       if (*c.abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > c.limit) {
         report_error(c, kErrTimeout, site);
         return false;
       }

@@ -215,10 +215,10 @@ fa_status check_common(int B, int H, int N, int d, float scale, const fa_options
   if (B < 1 || H < 1 || N < 1 || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (N > kStdMaxN || d < 8 || d > 256 || (d % 8) != 0) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H * N > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;   // one warp per row
-  bool dropout = false;
-  const int so = internal_read_options(options, f16, &dropout);
+  bool flash_only = false;   // dropout, tile record and test stall belong to the flash kernels
+  const int so = internal_read_options(options, f16, &flash_only);
   if (so != FA_OK) return (fa_status)so;
-  if (dropout) return FA_ERR_UNSUPPORTED;
+  if (flash_only) return FA_ERR_UNSUPPORTED;
   size_t total = 0;
   if (!ws_layout(B, H, N, s_bytes, &total)) return FA_ERR_UNSUPPORTED;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < total)

@@ -81,6 +81,27 @@ typedef enum {
  *           256 / (256 - t). The softmax statistics (LSE) use the undropped
  *           P. The backward call regenerates the same mask from the same
  *           p_drop and seed; nothing of the mask is stored.
+ *   tile_record: NULL (default), or a device uint8 [B, H, nT, nT] array that
+ *           the caller has zeroed. The kernels then record the tiles they
+ *           actually compute: for every (b, h, query tile qi, key tile kj)
+ *           that a kernel processes it adds 1 to byte
+ *           ((b * H + h) * nT + qi) * nT + kj when the tile needs no element
+ *           mask and 2 when it applies one; skipped tiles stay 0. A correct
+ *           run therefore reproduces flash_attn_tile_map's states per head,
+ *           and a tile computed twice would read 2 or 4. The forward and the
+ *           backward call each record into the array they are given (the
+ *           block-sparse skipping of the milestone page, "The idea", as the
+ *           kernels ran it). Costs one byte update per computed tile.
+ *   wait_limit_us: bound of every wait of a kernel on an on-chip barrier,
+ *           in microseconds; 0 (default) = 2 s. A wait that runs out makes
+ *           the kernel stop, free its on-chip resources and record
+ *           FA_ERR_DEVICE_TIMEOUT in the device error word.
+ *   test_stall: 0 (default). 1 is for testing the timeout path only: the
+ *           kernels' tile loader stops after its first tile, so that a
+ *           bounded wait runs out (after wait_limit_us) and the call's
+ *           outputs are unspecified; flash_attn_get_device_error then
+ *           returns FA_ERR_DEVICE_TIMEOUT. Nothing faults; the device stays
+ *           usable.
  */
 typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_F16 = 1 } fa_dtype;
 
@@ -90,6 +111,9 @@ typedef struct {
   float p_drop;
   uint32_t reserved;  /* 0 */
   uint64_t seed;
+  uint8_t* tile_record;
+  uint32_t wait_limit_us;
+  uint32_t test_stall;
 } fa_options;
 
 /*
@@ -169,7 +193,8 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
  * flash_attn_bwd computes (same arguments, minus the workspace) and takes
  * its scratch from a fixed array of FA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB)
  * that the library keeps on every device that loads it, until the process
- * exits. Neither it nor the library allocates anything.
+ * exits. This call allocates nothing (the baseline of standard_attn.h, which
+ * creates a cuBLAS handle, is another matter).
  *   - Shapes whose flash_attn_bwd_workspace_size exceeds
  *     FA_BWD_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_SCRATCH_LIMIT
  *     before anything is launched.
@@ -180,7 +205,13 @@ fa_status flash_attn_bwd_ex(const void* Q, const void* K, const void* V, const v
  *     previous call left there does not matter.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture
- *     starts.
+ *     starts. Under CUDA's default lazy module loading that first call is
+ *     also when the array is reserved on the device, so make it where
+ *     allocation is still allowed (a call refused with FA_ERR_SCRATCH_LIMIT
+ *     does as a warm-up, since the lookup comes before the size check), or
+ *     set CUDA_MODULE_LOADING=EAGER.
+ *   - Profile events set with flash_attn_set_profile_events apply to this
+ *     call as to flash_attn_bwd (around the backward main kernel).
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

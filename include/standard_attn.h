@@ -63,8 +63,8 @@ size_t standard_attn_workspace_size(int B, int H, int N);
  *             the row sum of exp(S) over the allowed keys)
  *   B, H >= 1; 1 <= N <= 65536; d a multiple of 8 in [8, 256]; scale finite;
  *   causal 0 or 1; kv_len, block_mask as in flash_attn.h (may be NULL).
- *   options: NULL or an fa_options; only dtype is used, p_drop must be 0
- *            (FA_ERR_UNSUPPORTED otherwise).
+ *   options: NULL or an fa_options; only dtype is used; p_drop must be 0,
+ *            tile_record NULL and test_stall 0 (FA_ERR_UNSUPPORTED otherwise).
  *   flags:   0 or STANDARD_ATTN_S16 (FA_ERR_INVALID_ARG otherwise).
  *   workspace: at least standard_attn_workspace_size(B, H, N) bytes,
  *            256-byte aligned (FA_ERR_WORKSPACE otherwise).

@@ -100,6 +100,29 @@ def test_options_validated_before_any_launch(lib):
     ws = L.flash_attn_bwd_workspace_size(1, 1, 128, 64)
     args = [p] * 9 + [1, 1, 128, 64, 0.1, 0, None, None]
     assert L.flash_attn_bwd_ex(*args, bad_dtype, p, ws, None) == 2
+    bad_stall = L.fa_options(test_stall=2)
+    assert L.flash_attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, bad_stall, None) == 1
+    assert L.flash_attn_bwd_ex(*args, bad_stall, p, ws, None) == 1
+
+
+def test_options_struct_layout(lib):
+    """The ctypes mirror has the C layout: the checking fields follow the
+    seed, and an older caller's shorter size keeps them at their defaults."""
+    from exact_io_aware_39_gb300 import _lib as L
+    import ctypes as C
+    assert C.sizeof(L.fa_options) == 40
+    assert L.fa_options.tile_record.offset == 24
+    assert L.fa_options.wait_limit_us.offset == 32 and L.fa_options.test_stall.offset == 36
+    p = C.c_void_p(1 << 20)
+    old = L.fa_options(test_stall=7)   # invalid stall, but outside a 24-byte struct
+    old.size = 24
+    bad_dtype = L.fa_options(7)
+    bad_dtype.size = 24
+    assert L.flash_attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, bad_dtype, None) == 2
+    # the validation of the forward with the short struct gets past the options
+    # (it then fails only at the device check, which needs a GPU)
+    st = L.flash_attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 64, 0.1, 0, None, None, old, None)
+    assert st != 1
 
 
 def test_standard_workspace_size_formula(lib):
@@ -124,6 +147,8 @@ def test_standard_attn_arguments_validated_before_any_launch(lib):
     assert fwd(q=None) == 1 and fwd(q=bad) == 1 and fwd(causal=2) == 1 and fwd(scale=float("nan")) == 1
     assert fwd(d=60) == 2 and fwd(d=264) == 2 and fwd(N=65537) == 2 and fwd(flags=2) == 1
     assert fwd(opts=L.fa_options(p_drop=0.1)) == 2        # dropout is not part of the baseline
+    assert fwd(opts=L.fa_options(tile_record=1 << 20)) == 2   # nor the flash kernels' tile record
+    assert fwd(opts=L.fa_options(test_stall=1)) == 2
     assert fwd(opts=L.fa_options(7)) == 2
     assert fwd(nbytes=ws - 1) == 3 and fwd(w=None) == 3 and fwd(w=ctypes.c_void_p((1 << 20) + 16)) == 3
     assert L.standard_attn_bwd(p, p, p, p, p, p, None, 1, 1, 128, 64, 0.1, None, 0, p, ws, None) == 1

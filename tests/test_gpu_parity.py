@@ -73,15 +73,23 @@ def _compare(got, ref, heads=None, with_bwd=True, o_tol=O_TOL, o_rel=0.0):
     fin = np.isfinite(r_lse)
     lse_err = np.abs(g_lse[fin] - r_lse[fin]).max() if fin.any() else 0.0
     errs = dict(O=o_err, LSE=lse_err)
-    assert o_err <= o_tol, errs
-    assert lse_err <= LSE_TOL, errs
     if with_bwd:
         for name in ("dQ", "dK", "dV"):
             r, g = ref[name][bi, hi], got[name][bi, hi]
             nr = np.linalg.norm(r)
-            rel = np.linalg.norm(g - r) / nr if nr > 0 else np.linalg.norm(g)
-            errs[name] = rel
-            assert rel <= GRAD_TOL, errs
+            errs[name] = np.linalg.norm(g - r) / nr if nr > 0 else np.linalg.norm(g)
+    # measured errors next to their bounds (visible with pytest -s), so that
+    # the slack of every case is on record
+    o_bound = f"{o_tol:g}" + (f" + {o_rel:.3g}|O_ref|" if o_rel else "")
+    print(f"PARITY O {o_diff.max():.3e} (excess over the |O_ref| term {o_err:.3e}, bound {o_bound}) "
+          f"LSE {lse_err:.3e} (bound {LSE_TOL:g})"
+          + "".join(f" {n} {errs[n]:.3e}" for n in ("dQ", "dK", "dV") if n in errs)
+          + (f" (bound {GRAD_TOL:g})" if with_bwd else ""))
+    assert o_err <= o_tol, errs
+    assert lse_err <= LSE_TOL, errs
+    if with_bwd:
+        for name in ("dQ", "dK", "dV"):
+            assert errs[name] <= GRAD_TOL, errs
     return errs
 
 
@@ -234,6 +242,83 @@ def test_tile_map_bit_exact(fa, spec):
     got = fa.tile_map(c["B"], c["N"], c["causal"], kv, bm).cpu().numpy()
     want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
     assert np.array_equal(got, want)
+
+
+def _recorded_tiles(fa, c):
+    """The tiles the forward and the backward kernels computed, as recorded
+    through fa_options.tile_record: two uint8 arrays [B, H, nT, nT]."""
+    dev = torch.device("cuda:0")
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    kv = None if c["kv_len"] is None else c["kv_len"].to(dev)
+    bm = None if c["block_mask"] is None else c["block_mask"].to(dev)
+    B, H, N = q.shape[:3]
+    nT = (N + 127) // 128
+    rec_f = torch.zeros((B, H, nT, nT), dtype=torch.uint8, device=dev)
+    rec_b = torch.zeros_like(rec_f)
+    o, lse = fa.attention_fwd(q, k, v, c["scale"], c["causal"], kv, bm, tile_record=rec_f)
+    fa.attention_bwd(q, k, v, o, do, lse, c["scale"], c["causal"], kv, bm, tile_record=rec_b)
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    return rec_f.cpu().numpy(), rec_b.cpu().numpy()
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=[s[0] for s in SMALL])
+def test_kernels_compute_exactly_the_classified_tiles(fa, spec):
+    """The tile-skip set as the kernels ran it: every (b, h, qi, kj) the
+    forward and the backward kernel computed, recorded by the thread that
+    decides on element masking (1 unmasked, 2 masked, summed over visits),
+    equals the oracle's tile states for every head, bit for bit; a skipped
+    tile that was computed, a masked tile computed without masking, or a tile
+    computed twice would all differ."""
+    c = _small_case(*spec)
+    rec_f, rec_b = _recorded_tiles(fa, c)
+    want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
+    want = np.broadcast_to(want[:, None], rec_f.shape)
+    assert np.array_equal(rec_f, want)
+    assert np.array_equal(rec_b, want)
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_workload_kernels_compute_exactly_the_classified_tiles(fa, name):
+    """The same record on the five workloads in their bench launch
+    configuration (heads reduced where the record would not change: the
+    states are shared by all heads; long_causal keeps its 128 x 128 grid)."""
+    w = WORKLOADS[name]
+    c = make_case(w, H=min(w.H, 2))
+    rec_f, rec_b = _recorded_tiles(fa, c)
+    want = oracle.tile_states(c["B"], w.N, w.causal, c["kv_len"], c["block_mask"])
+    want = np.broadcast_to(want[:, None], rec_f.shape)
+    assert np.array_equal(rec_f, want)
+    assert np.array_equal(rec_b, want)
+
+
+def test_plain_signatures_match_oracle(fa):
+    """flash_attn_fwd and flash_attn_bwd themselves (the calls without
+    options), through ctypes with raw device pointers, on a case with every
+    mask kind and a ragged tail."""
+    c = _small_case("plain_abi", 2, 2, 700, 64, True, [650, 300], "rand")
+    dev = torch.device("cuda:0")
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    kv, bm = c["kv_len"].to(dev), c["block_mask"].to(dev)
+    B, H, N, d = q.shape
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    need = fa.flash_attn_bwd_workspace_size(B, H, N, d)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=dev)
+    P = fa._lib._ptr
+    s = fa._lib._stream(None)
+    st = fa.flash_attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, c["scale"], 1, P(kv), P(bm), s)
+    assert st == 0
+    st = fa.flash_attn_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv), B, H, N, d, c["scale"], 1,
+                           P(kv), P(bm), P(ws), need, s)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    got = {n: t.float().cpu().numpy() for n, t in dict(O=o, LSE=lse, dQ=dq, dK=dk, dV=dv).items()}
+    ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], c["scale"], True, c["kv_len"],
+                                   c["block_mask"])
+    _compare(got, ref)
 
 
 FP16 = [s for s in SMALL if s[0] in ("tiny_noncausal", "ragged_causal", "d128_causal_ragged",
