@@ -149,7 +149,7 @@ fa_status read_options(const fa_options* opt, Options* out) {
 fa_status check_shape(int B, int H, int N, int d, float scale, int causal) {
   if (B < 1 || H < 1 || N < 1 || !std::isfinite(scale) || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
-  if (d < 8 || d > 128 || (d % 8) != 0) return FA_ERR_UNSUPPORTED;
+  if (d < 8 || d > kMaxHeadDim || (d % 8) != 0) return FA_ERR_UNSUPPORTED;
   if (N > kMaxN) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
   const long long nT = (N + kTile - 1) / kTile;
@@ -197,6 +197,7 @@ int internal_bwd_validate(const BwdArgs& a, const void* options) {
   if (st != FA_OK) return st;
   Options o;
   if ((st = read_options(static_cast<const fa_options*>(options), &o)) != FA_OK) return st;
+  if (o.drop.t != 0u && a.d > 128) return FA_ERR_UNSUPPORTED;   // no dropout in the wide kernels
   const void* ptrs[] = {a.Q, a.K, a.V, a.O, a.dO, a.LSE, a.dQ, a.dK, a.dV};
   for (const void* q : ptrs)
     if (q == nullptr || !aligned16(q)) return FA_ERR_INVALID_ARG;
@@ -224,8 +225,9 @@ int internal_bwd_run(const BwdArgs& a, const void* options, void* workspace, voi
   unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-  if (make_map(&tq, a.Q, BH, N, d, o.f16) || make_map(&tk, a.K, BH, N, d, o.f16) ||
-      make_map(&tv, a.V, BH, N, d, o.f16) || make_map(&tdo, a.dO, BH, N, d, o.f16) ||
+  const int qrows = kernel_head_dim(d) == 256 ? 64 : kTile;   // the wide backward takes 64 queries at a time
+  if (make_map(&tq, a.Q, BH, N, d, o.f16, qrows) || make_map(&tk, a.K, BH, N, d, o.f16) ||
+      make_map(&tv, a.V, BH, N, d, o.f16) || make_map(&tdo, a.dO, BH, N, d, o.f16, qrows) ||
       make_map(&tdk, a.dK, BH, N, d, o.f16, 32) || make_map(&tdv, a.dV, BH, N, d, o.f16, 32) ||
       make_dq_map(&tdq, dq_acc, BH, nT * kTile, d))
     return FA_ERR_CUDA;
@@ -278,6 +280,7 @@ fa_status flash_attn_fwd_ex(const void* Q, const void* K, const void* V, void* O
   if (st != FA_OK) return st;
   Options o;
   if ((st = read_options(options, &o)) != FA_OK) return st;
+  if (o.drop.t != 0u && d > 128) return FA_ERR_UNSUPPORTED;   // no dropout in the wide kernels
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return FA_ERR_INVALID_ARG;

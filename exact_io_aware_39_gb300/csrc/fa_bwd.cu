@@ -768,7 +768,7 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
                            float* delta, unsigned int* sched, int BH, int N, int nT, int d, cudaStream_t s) {
   const int Np = nT * kTile;
   int G = 1;
-  while (G < d / 8) G <<= 1;              // 1 .. 16: divides the block and the warp
+  while (G < d / 8) G <<= 1;              // 1 .. 32: divides the block and the warp
   const long long threads = (long long)BH * Np * G;
   const int block = 256;
   const unsigned grid = (unsigned)((threads + block - 1) / block);
@@ -787,6 +787,7 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
   FA_PRE_CASE(4)
   FA_PRE_CASE(8)
   FA_PRE_CASE(16)
+  FA_PRE_CASE(32)
 #undef FA_PRE_CASE
   return cudaErrorInvalidValue;
 }
@@ -797,6 +798,7 @@ cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtens
   const float scale = p.scale_log2 / 1.4426950408889634f;
   const bool drop = p.drop.t > 0;
   const int kd = kernel_head_dim(d);
+  if (kd == 256) return drop ? cudaErrorInvalidValue : launch_bwd_wide(f16, tq, tk, tv, tdo, tdk, tdv, tdq, p, s);
 #define FA_BWD_CASE(DD, FF, DR) \
   if (kd == DD && f16 == FF && drop == DR) \
     return launch_bwd_main_d<DD, FF, DR>(tq, tk, tv, tdo, tdk, tdv, tdq, p, scale, s);

@@ -145,9 +145,10 @@ cudaError_t once_per_device(PerDeviceOnce& o, int dev, F&& f) {
 }
 
 // Head dimension of the kernel that serves a head dimension d (a multiple of
-// 8 up to 128): tiles are 64 or 128 columns wide; columns past d are zeros on
-// load (TMA out-of-bounds fill) and are not written on store.
-__host__ __device__ __forceinline__ int kernel_head_dim(int d) { return d <= 64 ? 64 : 128; }
+// 8 up to 256): tiles are 64, 128 or 256 columns wide; columns past d are
+// zeros on load (TMA out-of-bounds fill) and are not written on store.
+__host__ __device__ __forceinline__ int kernel_head_dim(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+constexpr int kMaxHeadDim = 256;
 
 // Launchers (host). Tensor maps are 3-D [BH, N, d] bf16 views, box 64 x 128 x 1
 // for loads and 64 x 32 x 1 for the stores of O, dK and dV (one box per warp),
@@ -169,6 +170,14 @@ cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtens
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tdq,
                             const BwdParams& p, cudaStream_t s);
+
+// The kernels for 128 < d <= 256 (fa_wide.cu; no dropout). The backward's
+// tq and tdo are views with 64-row boxes (queries are taken 64 at a time).
+cudaError_t launch_fwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                            const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s);
 
 cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, int BH, int N, int nT, int d,
                           cudaStream_t s);

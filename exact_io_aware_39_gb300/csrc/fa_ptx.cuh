@@ -297,6 +297,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kstep) {
   return sdesc_sw128(tile + (uint32_t)kstep * 2048u, 16384u, 1024u);
 }
 
+// The same two layouts for tiles whose 64-element atoms are `atom` bytes
+// apart (8 KB for a 64-row tile as TMA writes a [64 x 64] box): K-major with
+// the k-th step in atom k / 4; MN-major with 64-wide MN chunks `atom` apart.
+__device__ __forceinline__ uint64_t desc_kmajor_at(uint32_t tile, int kstep, uint32_t atom) {
+  return sdesc_sw128(tile + (uint32_t)(kstep >> 2) * atom + (uint32_t)(kstep & 3) * 32u, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor_at(uint32_t tile, int kstep, uint32_t atom) {
+  return sdesc_sw128(tile + (uint32_t)kstep * 2048u, atom, 1024u);
+}
+
 // Per-step descriptor increments (in the 16-byte units of the address
 // field) for the layouts above, so that a loop can add a constant to a base
 // descriptor computed once: K-major step k -> atom k / 4 (16 KB) plus 32 bytes

@@ -58,7 +58,8 @@ def test_workspace_size_formula(lib):
         want = al(al(B * H * Np * d * 4) + B * H * Np * 4) + al(B * H * Np * 4) + 256
         assert L.flash_attn_bwd_workspace_size(B, H, N, d) == want
     assert L.flash_attn_bwd_workspace_size(1, 1, 256, 96) == al(al(256 * 96 * 4) + 256 * 4) + al(256 * 4) + 256
-    for bad_d in (0, 4, 60, 136, 256):
+    assert L.flash_attn_bwd_workspace_size(1, 1, 256, 256) == al(al(256 * 256 * 4) + 256 * 4) + al(256 * 4) + 256
+    for bad_d in (0, 4, 60, 136 + 4, 264, 512):
         assert L.flash_attn_bwd_workspace_size(1, 1, 256, bad_d) == 0
     assert L.flash_attn_bwd_workspace_size(0, 1, 256, 64) == 0
 
@@ -66,7 +67,7 @@ def test_workspace_size_formula(lib):
 @pytest.mark.parametrize("B,H,N,d,scale,causal,want", [
     (0, 1, 128, 64, 0.1, 0, 1), (1, 0, 128, 64, 0.1, 0, 1), (1, 1, 0, 64, 0.1, 0, 1),
     (1, 1, 128, 64, float("nan"), 0, 1), (1, 1, 128, 64, float("inf"), 0, 1),
-    (1, 1, 128, 64, 0.1, 2, 1), (1, 1, 128, 60, 0.1, 0, 2), (1, 1, 128, 136, 0.1, 0, 2),
+    (1, 1, 128, 64, 0.1, 2, 1), (1, 1, 128, 60, 0.1, 0, 2), (1, 1, 128, 264, 0.1, 0, 2),
     (1, 1, 128, 0, 0.1, 0, 2), (1, 1, 131073, 64, 0.1, 0, 2),
 ])
 def test_invalid_shapes_rejected_before_any_launch(lib, B, H, N, d, scale, causal, want):

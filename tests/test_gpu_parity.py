@@ -153,6 +153,8 @@ MANY_ITEMS = [
     ("many_items_d128_kv_len", 2, 384, 128, False, [384, 200], None),
     ("many_items_block_mask", 2, 512, 64, False, None, "rand"),
     ("many_items_d96_all_masks", 2, 640, 96, True, [600, 333], "rand"),
+    ("many_items_d256_kv_len_causal", 4, 512, 256, True, [512, 0, 300, 129], None),
+    ("many_items_d192_block_mask", 2, 512, 192, False, None, "rand"),
 ]
 
 
@@ -184,6 +186,18 @@ HEAD_DIMS = [
     ("d72", 1, 2, 384, 72, False, None, None),
     ("d96_causal_block_mask", 1, 2, 640, 96, True, None, "rand"),
     ("d120_all_masks", 2, 2, 700, 120, True, [650, 300], "rand"),
+    # above 128: the wide kernels (one Q tile per forward CTA; the backward
+    # split over the two halves of the head dimension)
+    ("d136_causal_ragged", 1, 2, 333, 136, True, None, None),
+    ("d160_causal", 1, 2, 640, 160, True, None, None),
+    ("d160_kv_len", 3, 2, 300, 160, False, [300, 5, 130], None),
+    ("d192_block_mask", 2, 2, 768, 192, False, None, "rand"),
+    ("d192_causal_block_mask", 1, 2, 640, 192, True, None, "rand"),
+    ("d256", 1, 2, 384, 256, False, None, None),
+    ("d256_causal_kv_len", 3, 2, 520, 256, True, [520, 77, 300], None),
+    ("d256_block_mask_empty_rows", 1, 2, 512, 256, False, None, "rows"),
+    ("d248_all_masks", 2, 2, 700, 248, True, [650, 300], "rand"),
+    ("d256_n1", 2, 2, 1, 256, False, None, None),
 ]
 
 
@@ -196,11 +210,32 @@ def test_head_dims_match_oracle(fa, spec):
     _compare(got, ref, o_rel=HEAD_DIM_O_REL)
 
 
-def test_head_dim_96_fp16(fa):
-    c = _small_case("d96_fp16", 1, 2, 384, 96, True, None, None, dtype=torch.float16)
+@pytest.mark.parametrize("d", [96, 256])
+def test_head_dim_fp16(fa, d):
+    c = _small_case(f"d{d}_fp16", 1, 2, 384, d, True, None, None, dtype=torch.float16)
     got = _run_gpu(fa, c)
     ref = oracle.attention_fwd_bwd(c["q"], c["k"], c["v"], c["do"], c["scale"], c["causal"])
     _compare(got, ref, o_rel=HEAD_DIM_O_REL)
+
+
+@pytest.mark.parametrize("spec", [h for h in HEAD_DIMS if h[4] > 128], ids=[h[0] for h in HEAD_DIMS if h[4] > 128])
+def test_wide_kernels_compute_exactly_the_classified_tiles(fa, spec):
+    """The tile record of the wide kernels (d > 128) against the oracle's
+    tile states, as for the narrower kernels."""
+    c = _small_case(*spec)
+    rec_f, rec_b = _recorded_tiles(fa, c)
+    want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
+    want = np.broadcast_to(want[:, None], rec_f.shape)
+    assert np.array_equal(rec_f, want)
+    assert np.array_equal(rec_b, want)
+
+
+def test_wide_head_dims_refuse_dropout(fa):
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, 1, 128, 256, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fa.FlashAttnError):
+        fa.attention_fwd(q, q, q, 0.1, p_drop=0.1)
+    assert fa.device_error()[0] == 0
 
 
 MAX_LEN = [
@@ -467,7 +502,7 @@ def test_invalid_arguments_on_device(fa):
     lse = torch.zeros(1, 1, 128, dtype=torch.float32, device=dev)
     P = fa._lib._ptr
     s = fa._lib._stream(None)
-    for bad_d in (60, 136):   # rejected before anything is launched
+    for bad_d in (60, 264):   # rejected before anything is launched
         assert fa.flash_attn_fwd(P(q), P(q), P(q), P(q), P(lse), 1, 1, 128, bad_d, 0.1, 0, None, None, s) == 2
     mis = torch.zeros(1 + 128 * 64, dtype=torch.bfloat16, device=dev)[1:]
     assert fa.flash_attn_fwd(P(mis), P(q), P(q), P(q), P(lse), 1, 1, 128, 64, 0.1, 0, None, None, s) == 1

@@ -45,7 +45,7 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype in (torch.bfloat16, torch.float16) else t.view(torch.int32)
 
 
-@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False), (256, True)])
 def test_forward_wait_runs_out_and_device_stays_usable(fa, d, causal):
     w, (q, k, v, _) = _inputs(d, causal)
     assert fa.device_error()[0] == 0
@@ -64,7 +64,7 @@ def test_forward_wait_runs_out_and_device_stays_usable(fa, d, causal):
     assert torch.equal(_bits(o1), _bits(o0)) and torch.equal(_bits(l1), _bits(l0))
 
 
-@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False), (256, True)])
 def test_backward_wait_runs_out_and_device_stays_usable(fa, d, causal):
     w, (q, k, v, do) = _inputs(d, causal)
     o, lse = fa.attention_fwd(q, k, v, w.scale, causal)
