@@ -98,13 +98,13 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// 3-D view [BH, Np, d] of the fp32 dQ accumulator, box 32 x 32 x 1 (one
-// 128-byte row per box row; each warp adds its own 32 query rows), 128-byte
-// swizzle.
-fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d) {
+// 3-D view [BH, Np, d] of the fp32 dQ accumulator, box 32 x rows x 1 (one
+// 128-byte row per box row), 128-byte swizzle: whole 128-row tiles for the
+// narrow backward, 32 rows (each warp its own) for the wide one.
+fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d, int rows) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Np, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)Np * d * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {32, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -225,11 +225,13 @@ int internal_bwd_run(const BwdArgs& a, const void* options, void* workspace, voi
   unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-  const int qrows = kernel_head_dim(d) == 256 ? 64 : kTile;   // the wide backward takes 64 queries at a time
+  const bool wide = kernel_head_dim(d) == 256;
+  const int qrows = wide ? 64 : kTile;    // the wide backward takes 64 queries at a time
+  const int srows = wide ? 32 : kTile;    // and stores dK, dV per warp (32 rows); the narrow one a whole tile
   if (make_map(&tq, a.Q, BH, N, d, o.f16, qrows) || make_map(&tk, a.K, BH, N, d, o.f16) ||
       make_map(&tv, a.V, BH, N, d, o.f16) || make_map(&tdo, a.dO, BH, N, d, o.f16, qrows) ||
-      make_map(&tdk, a.dK, BH, N, d, o.f16, 32) || make_map(&tdv, a.dV, BH, N, d, o.f16, 32) ||
-      make_dq_map(&tdq, dq_acc, BH, nT * kTile, d))
+      make_map(&tdk, a.dK, BH, N, d, o.f16, srows) || make_map(&tdv, a.dV, BH, N, d, o.f16, srows) ||
+      make_dq_map(&tdq, dq_acc, BH, nT * kTile, d, wide ? 32 : kTile))
     return FA_ERR_CUDA;
   if (launch_bwd_pre(o.f16, a.O, a.dO, a.LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
     return FA_ERR_CUDA;

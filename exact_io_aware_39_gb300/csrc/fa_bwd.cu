@@ -79,7 +79,7 @@ struct BwdLayout {
   static constexpr int bQFull = bKV + kKV;
   static constexpr int bQEmpty = bQFull + kStages;
   static constexpr int bdOFull = bQEmpty + kStages;        // [stages]
-  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA (4 arrivals)
+  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA
   static constexpr int bSFull = bdOFree + kStages;
   static constexpr int bPFull = bSFull + 1;
   static constexpr int bdPFull = bPFull + 1;
@@ -89,7 +89,7 @@ struct BwdLayout {
   static constexpr int bdQFree = bdQFull + 1;
   static constexpr int bFinal = bdQFree + 1;
   static constexpr int bDrain = bFinal + 1;
-  static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (8 arrivals)
+  static constexpr int bKVFree = bDrain + 1;   // [kKV]: the epilogue's staging has been read (2 arrivals)
   // work items reach the other roles through a ring filled by the producer
   static constexpr int kItemRing = 4;
   static constexpr int bItemFull = bKVFree + kKV;            // [kItemRing]
@@ -179,9 +179,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
       mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u
-                        : i == L::bdQFree ? 4u
-                        : (i >= L::bdOFree && i < L::bdOFree + L::kStages) ? 4u     // the four drain warps
-                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 8u         // the eight compute warps
+                        : i == L::bdQFree ? 4u                                       // the four drain warps
+                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 2u         // one thread per compute group
                         : i >= L::bItemEmpty ? 13u : 1u);   // arrivals
     *abort_flag = 0u;
     fence_mbar_init();
@@ -190,6 +189,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
+  // global memory is read and written only from here on: what the pre-pass
+  // wrote (row statistics, zeroed accumulator and work counter) is visible
+  grid_dep_wait();
+  grid_dep_launch();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -387,21 +390,27 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const float sl2 = p.scale_log2;
     bool ok = true;
     int g = 0, nf = 0;
-    int pending = -1;   // K/V buffer whose epilogue stores have not been waited for yet
-    // the stores out of buffer `pending` have read its staging (each warp
-    // waits for its own): the buffer goes back to the producer
+    int pending = -1;   // K/V buffer whose epilogue store has not been waited for yet (thread r == 0)
+    // the store out of buffer `pending` has read its staging: the buffer goes
+    // back to the producer
     auto release_kv = [&]() {
       if (pending >= 0) {
-        if (lane == 0) {
+        if (r == 0) {
           bulk_wait_group_read_all();
           mbar_arrive(bar(L::bKVFree + pending));
         }
         pending = -1;
       }
     };
+    // The four warps of a group meet at a named barrier in each item's
+    // epilogue; before it, and wherever one of them may have stopped (a wait
+    // that ran out or saw the abort flag), they agree with group_all, so that
+    // all of them take the same branch and none waits for one that has left.
+    const uint32_t gbar = 1u + (uint32_t)cw;
     for (int k = 0; ok; ++k) {
       const int item = take_item(k, true, ok);
-      if (item < 0) break;
+      ok = group_all(gbar, 128, ok);
+      if (!ok || item < 0) break;
       const Item w = item_at(item);
       const int krow = kTile * w.kj + r;
       int i = next_live(w, 0);
@@ -529,12 +538,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK, for every key
       // row of the tile (zeros when no query tile was live), staged in the
       // item's V or K buffer once every MMA has read it, and stored by TMA
-      ok = __all_sync(0xFFFFFFFFu, ok);
+      ok = group_all(gbar, 128, ok);
       if (!ok) break;
       release_kv();   // the buffer of an earlier item without live query tiles
       const int kb = k % L::kKV;
-      if (!(ok = mbar_wait_warp(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 124))) break;
-      if (live && !(ok = mbar_wait_warp(bar(L::bFinal), (uint32_t)nf & 1u, ctl, 125))) break;
+      ok = mbar_wait_warp(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 124);
+      if (ok && live) ok = mbar_wait_warp(bar(L::bFinal), (uint32_t)nf & 1u, ctl, 125);
+      ok = group_all(gbar, 128, ok);
+      if (!ok) break;
       nf += live ? 1 : 0;
       tc_fence_after();
       const uint32_t tacc = (cw == 0 ? tdV : tdK) + lane_off;
@@ -561,33 +572,29 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
         }
       }
-      // each warp stores its own 32 key rows (boxes of 32 rows), so that no
-      // warp ever waits for another at a group-wide barrier
       tc_fence_before();
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int row0 = kTile * w.kj + 32 * (warp & 3);
-        if (row0 < p.N)
-          for (int h = 0; h < L::kHalves; ++h)
-            tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384 + 4096 * (warp & 3), 64 * h, row0,
-                         w.bh);
+      named_bar_sync(gbar, 128);
+      if (r == 0) {
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
         bulk_commit_group();
       }
       pending = kb;
       // with one K/V buffer the next item's K and V wait for this store
       if (L::kKV == 1) release_kv();
     }
-    if (lane == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
+    if (r == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
-    // has completed) in two rounds of 32-column boxes, 128-byte swizzled ->
-    // TMA reduce-add into the accumulator; each warp adds its own 32 query
-    // rows (boxes of 32 rows x 32 fp32) and synchronises only within itself.
-    // The TMEM columns are released as soon as they are all in registers or
-    // staged; the slot goes back to the producer when all four warps' last
-    // round has been read.
+    // has completed) in two rounds of boxes of [128 rows x 32 fp32], 128-byte
+    // swizzled -> TMA reduce-add into the accumulator. The TMEM columns are
+    // released as soon as they are all in registers or staged; the slot goes
+    // back to the producer when the last round has been read. The four warps
+    // meet at named barriers in every round; after each wait that one of them
+    // may fail they agree with group_all, so that they always take the same
+    // branch.
     regs_dec<kDrainRegs>();
     constexpr int kBoxesPerRound = L::kTileBytes / 16384;    // 1 (d = 64) or 2 (d = 128)
     constexpr int kRounds = D / 32 / kBoxesPerRound;
@@ -598,12 +605,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     int g = 0;
     for (int k = 0; ok; ++k) {
       const int item = take_item(k, true, ok);
-      if (item < 0) break;
+      ok = group_all(3, 128, ok);
+      if (!ok || item < 0) break;
       const Item w = item_at(item);
       for (int i = next_live(w, 0); i < p.nT; ++g, i = next_live(w, i + 1)) {
         const int s = g % L::kStages;
         const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
-        if (!(ok = mbar_wait_warp(bar(L::bdQFull), (uint32_t)g & 1u, ctl, 130))) break;
+        ok = mbar_wait_warp(bar(L::bdQFull), (uint32_t)g & 1u, ctl, 130);
+        if (!(ok = group_all(3, 128, ok))) break;
         tc_fence_after();
         uint32_t u[kBoxesPerRound][32];
 #pragma unroll
@@ -616,9 +625,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             tc_fence_before();
             mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
           }
-          if (round > 0) {              // this warp's previous round has been read out of the slot
-            if (lane == 0) bulk_wait_group_read_all();
-            __syncwarp();
+          if (round > 0) {              // the previous round has been read out of the slot
+            if (r == 0) bulk_wait_group_read_all();
+            named_bar_sync(3, 128);
           }
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b)
@@ -629,13 +638,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                   make_uint4(u[b][4 * k8], u[b][4 * k8 + 1], u[b][4 * k8 + 2], u[b][4 * k8 + 3]);
             }
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
+          named_bar_sync(3, 128);
+          if (r == 0) {
 #pragma unroll
             for (int b = 0; b < kBoxesPerRound; ++b)
               if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
-                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b + 4096u * (uint32_t)(warp & 3),
-                                  32 * (round * kBoxesPerRound + b), kTile * i + 32 * (warp & 3), w.bh);
+                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b),
+                                  kTile * i, w.bh);
             bulk_commit_group();
           }
           if (round + 1 < kRounds) {    // the next columns into registers while the round is read
@@ -646,13 +655,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
           }
         }
-        if (lane == 0) {
+        if (r == 0) {
           bulk_wait_group_read_all();
           mbar_arrive(bar(L::bdOFree + s));
         }
       }
     }
-    if (lane == 0) bulk_wait_group_all();     // reductions complete before exit
+    if (r == 0) bulk_wait_group_all();     // reductions complete before exit
   }
 
   tc_fence_before();
@@ -672,6 +681,8 @@ __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t
                                   const float* __restrict__ lse, float* __restrict__ dq_acc,
                                   float* __restrict__ lse2, float* __restrict__ delta,
                                   unsigned int* __restrict__ sched, int BH, int N, int Np, int d) {
+  grid_dep_wait();   // O and LSE of the forward kernel are complete
+  grid_dep_launch();
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid == 0) *sched = 0u;
   const long long row = gid / G;           // over BH * Np
@@ -716,6 +727,8 @@ __global__ void fa_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t
 template <bool F16>
 __global__ void fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, float scale,
                                  int BH, int N, int Np, int d) {
+  grid_dep_wait();   // every partial of the main kernel has been added
+  grid_dep_launch();
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int parts = d / 8;
   const long long total = (long long)BH * N * parts;
@@ -758,8 +771,8 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
-  fa_bwd_main_kernel<D, F16, DROP><<<grid, kBwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
-  return cudaGetLastError();
+  return launch_pdl(fa_bwd_main_kernel<D, F16, DROP>, grid, dim3(kBwdThreads), L::kSmemBytes, s, tq, tk, tv, tdo,
+                    tdk, tdv, tdq, q, scale);
 }
 
 }  // namespace
@@ -774,14 +787,10 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
   const unsigned grid = (unsigned)((threads + block - 1) / block);
   const uint16_t* o16 = static_cast<const uint16_t*>(o);
   const uint16_t* g16 = static_cast<const uint16_t*>(dout);
-#define FA_PRE_CASE(GG)                                                                                     \
-  if (G == GG) {                                                                                            \
-    if (f16)                                                                                                \
-      fa_bwd_pre_kernel<GG, true><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d); \
-    else                                                                                                    \
-      fa_bwd_pre_kernel<GG, false><<<grid, block, 0, s>>>(o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d); \
-    return cudaGetLastError();                                                                              \
-  }
+#define FA_PRE_CASE(GG)                                                                                       \
+  if (G == GG)                                                                                                \
+    return launch_pdl(f16 ? fa_bwd_pre_kernel<GG, true> : fa_bwd_pre_kernel<GG, false>, dim3(grid), dim3(block), 0, \
+                      s, o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d);
   FA_PRE_CASE(1)
   FA_PRE_CASE(2)
   FA_PRE_CASE(4)
@@ -821,11 +830,8 @@ cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, 
   const long long threads = (long long)BH * N * (d / 8);
   const int block = 256;
   const unsigned grid = (unsigned)((threads + block - 1) / block);
-  if (f16)
-    fa_bwd_dq_kernel<true><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
-  else
-    fa_bwd_dq_kernel<false><<<grid, block, 0, s>>>(dq_acc, static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
-  return cudaGetLastError();
+  return launch_pdl(f16 ? fa_bwd_dq_kernel<true> : fa_bwd_dq_kernel<false>, dim3(grid), dim3(block), 0, s, dq_acc,
+                    static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
 }
 
 }  // namespace fa

@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -144,6 +145,26 @@ cudaError_t once_per_device(PerDeviceOnce& o, int dev, F&& f) {
   return e;
 }
 
+// Launches a kernel with programmatic stream serialization: it may be
+// scheduled while the previous kernel in the stream is still running (once
+// that one allows it, or when its blocks exit), overlapping its launch and
+// set-up with the other's tail. Every kernel launched this way waits
+// (griddepcontrol.wait) before it touches global memory.
+template <typename... Exp, typename... Act>
+cudaError_t launch_pdl(void (*kern)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
+}
+
 // Head dimension of the kernel that serves a head dimension d (a multiple of
 // 8 up to 256): tiles are 64, 128 or 256 columns wide; columns past d are
 // zeros on load (TMA out-of-bounds fill) and are not written on store.
@@ -163,9 +184,9 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
                            float* lse2, float* delta, unsigned int* sched, int BH, int N, int nT, int d,
                            cudaStream_t s);
 
-// tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 32 x 1,
-// 128-byte swizzle; partial dQ tiles are added into it with TMA reduce-add,
-// each warp its own 32 query rows.
+// tdq is the fp32 dQ accumulator seen as [BH, nT*128, d], box 32 x 128 x 1
+// (32 x 32 x 1 for the wide kernel), 128-byte swizzle; partial dQ tiles are
+// added into it with TMA reduce-add.
 cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const CUtensorMap& tdq,

@@ -101,7 +101,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   int bh = 0;
   const int c = nC - 1 - split_grouped((int)blockIdx.x, p.group, nC, BH, &bh);
   const int b = bh / p.H;
-  const int kvl = effective_kv_len(p.kv_len, b, p.N);
   const int qi0 = 2 * c;
   const bool has_t1 = (qi0 + 1) < p.nT;
 
@@ -130,6 +129,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
+  // global memory is read and written only from here on: what the previous
+  // kernel in the stream wrote is complete and visible
+  grid_dep_wait();
+  grid_dep_launch();
+  const int kvl = effective_kv_len(p.kv_len, b, p.N);
   if (warp == 8) {
     // union list of live key tiles of the two Q tiles, ascending j
     int count = 0;
@@ -498,8 +502,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));
-  fa_fwd_kernel<D, F16, DROP><<<grid, kFwdThreads, L::kSmemBytes, s>>>(tq, tk, tv, to, q);
-  return cudaGetLastError();
+  return launch_pdl(fa_fwd_kernel<D, F16, DROP>, grid, dim3(kFwdThreads), L::kSmemBytes, s, tq, tk, tv, to, q);
 }
 
 }  // namespace

@@ -58,6 +58,28 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier with an AND-reduction: every one of the nthreads threads
+// arrives with a flag and all receive the AND of them. A group of warps that
+// decides with this before a group-wide barrier takes the same branch
+// everywhere, so that no warp can wait at a barrier that another has left.
+__device__ __forceinline__ bool group_all(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r) : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
+// Programmatic dependent launch: wait until the grid this one depends on (the
+// previous kernel in the stream) has completed and its writes are visible;
+// allow the next grid to be scheduled. Both are no-ops for a kernel launched
+// without the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

@@ -97,7 +97,6 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   int bh = 0;
   // groups of p.group heads whose K and V fit in L2 together; heaviest Q tiles first
   const int qi = p.nT - 1 - split_grouped((int)blockIdx.x, p.group, p.nT, BH, &bh);
-  const int kvl = effective_kv_len(p.kv_len, bh / p.H, p.N);
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -122,6 +121,9 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
+  grid_dep_wait();   // global memory only from here on (programmatic dependent launch)
+  grid_dep_launch();
+  const int kvl = effective_kv_len(p.kv_len, bh / p.H, p.N);
   if (warp == 4) {
     // live key tiles of this Q tile, ascending
     int count = 0;
@@ -521,6 +523,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
+  grid_dep_wait();   // global memory only from here on (programmatic dependent launch)
+  grid_dep_launch();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -860,8 +864,7 @@ cudaError_t launch_fwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& 
   FwdParams q = p;
   q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  kern<<<grid, kWFwdThreads, WFwdLayout::kSmemBytes, s>>>(tq, tk, tv, to, q);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kWFwdThreads), WFwdLayout::kSmemBytes, s, tq, tk, tv, to, q);
 }
 
 cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -883,8 +886,7 @@ cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& 
   const long long items = 2LL * p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
   const float scale = p.scale_log2 / 1.4426950408889634f;
-  kern<<<grid, kWBwdThreads, WBwdLayout::kSmemBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kWBwdThreads), WBwdLayout::kSmemBytes, s, tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
 }
 
 }  // namespace fa
