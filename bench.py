@@ -56,7 +56,8 @@ def _args():
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="element type of Q, K, V, dO (and of the outputs)")
     ap.add_argument("--shape", default=None,
-                    help="B,H,N override of the workload (smaller cases for profiler captures)")
+                    help="B,H,N or B,H,N,d override of the workload (smaller cases for profiler captures, "
+                         "other head dimensions)")
     ap.add_argument("--study", default=None, choices=["io", "memory"],
                     help="flash vs standard attention: time/FLOP/memory on one workload (io), or "
                          "extra device memory over N = 128..65536 (memory)")
@@ -243,8 +244,12 @@ def _resolve_workload(args, default):
     from exact_io_aware_39_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload or default]
     if args.shape:
-        sb, sh, sn = (int(x) for x in args.shape.split(","))
-        w = dataclasses.replace(w, B=sb, H=sh, N=sn, name=f"{w.name}@{sb}x{sh}x{sn}")
+        parts = [int(x) for x in args.shape.split(",")]
+        sb, sh, sn = parts[:3]
+        sd = parts[3] if len(parts) > 3 else w.d
+        name = f"{w.name}@{sb}x{sh}x{sn}" + (f"x{sd}" if sd != w.d else "")
+        scale = w.scale if sd == w.d else 1.0 / math.sqrt(sd)
+        w = dataclasses.replace(w, B=sb, H=sh, N=sn, d=sd, scale=scale, name=name)
     return w
 
 

@@ -115,7 +115,7 @@ fa_status make_dq_map(CUtensorMap* m, const float* base, int BH, int Np, int d, 
 struct Options {
   bool f16 = false;
   DropoutParams drop{0u, 0u, 0u, 1.0f};
-  CheckParams chk{nullptr, 2000000000ull, 0u};
+  CheckParams chk{nullptr, 2000000u, 0u};   // 2 s per wait
 };
 
 // Reads the caller's options (NULL = defaults). Fields beyond the caller's
@@ -138,7 +138,7 @@ fa_status read_options(const fa_options* opt, Options* out) {
   }
   if (opt->size >= offsetof(fa_options, tile_record) + sizeof(uint8_t*)) out->chk.rec = opt->tile_record;
   if (opt->size >= offsetof(fa_options, wait_limit_us) + sizeof(uint32_t) && opt->wait_limit_us != 0u)
-    out->chk.wait_ns = 1000ull * opt->wait_limit_us;
+    out->chk.wait_us = opt->wait_limit_us;
   if (opt->size >= offsetof(fa_options, test_stall) + sizeof(uint32_t)) {
     if (opt->test_stall > 1u) return FA_ERR_INVALID_ARG;
     out->chk.stall = opt->test_stall;
@@ -225,13 +225,17 @@ int internal_bwd_run(const BwdArgs& a, const void* options, void* workspace, voi
   unsigned int* sched = reinterpret_cast<unsigned int*>(ws + w.sched_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-  const bool wide = kernel_head_dim(d) == 256;
-  const int qrows = wide ? 64 : kTile;    // the wide backward takes 64 queries at a time
-  const int srows = wide ? 32 : kTile;    // and stores dK, dV per warp (32 rows); the narrow one a whole tile
+  const int kd = kernel_head_dim(d);
+  const int qrows = kd == 256 ? 64 : kTile;    // the wide backward takes 64 queries at a time
+  // the narrow kernels store dK and dV a whole tile at a time, the wide one per
+  // warp (32 rows); the dQ partials are added per warp (32 rows) except by the
+  // 64-column kernel, which adds whole 128-row tiles
+  const int srows = kd == 256 ? 32 : kTile;
+  const int dqrows = kd == 64 ? kTile : 32;
   if (make_map(&tq, a.Q, BH, N, d, o.f16, qrows) || make_map(&tk, a.K, BH, N, d, o.f16) ||
       make_map(&tv, a.V, BH, N, d, o.f16) || make_map(&tdo, a.dO, BH, N, d, o.f16, qrows) ||
       make_map(&tdk, a.dK, BH, N, d, o.f16, srows) || make_map(&tdv, a.dV, BH, N, d, o.f16, srows) ||
-      make_dq_map(&tdq, dq_acc, BH, nT * kTile, d, wide ? 32 : kTile))
+      make_dq_map(&tdq, dq_acc, BH, nT * kTile, d, dqrows))
     return FA_ERR_CUDA;
   if (launch_bwd_pre(o.f16, a.O, a.dO, a.LSE, dq_acc, lse2, delta, sched, BH, N, nT, d, s) != cudaSuccess)
     return FA_ERR_CUDA;

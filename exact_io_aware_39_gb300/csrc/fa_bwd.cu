@@ -79,7 +79,7 @@ struct BwdLayout {
   static constexpr int bQFull = bKV + kKV;
   static constexpr int bQEmpty = bQFull + kStages;
   static constexpr int bdOFull = bQEmpty + kStages;        // [stages]
-  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA
+  static constexpr int bdOFree = bdOFull + kStages;        // [stages]: dQ staging read by TMA (1 arrival, 4 per warp at d = 128)
   static constexpr int bSFull = bdOFree + kStages;
   static constexpr int bPFull = bSFull + 1;
   static constexpr int bdPFull = bPFull + 1;
@@ -95,9 +95,13 @@ struct BwdLayout {
   static constexpr int bItemFull = bKVFree + kKV;            // [kItemRing]
   static constexpr int bItemEmpty = bItemFull + kItemRing;   // [kItemRing]: MMA thread + 8 compute + 4 drain warps
   static constexpr int kNumBars = bItemEmpty + kItemRing;
-  static constexpr int kMisc = kBar + 8 * kNumBars;
-  static constexpr int kRing = kMisc + 16;                    // [kItemRing] item indices
-  static constexpr int kSmemBytes = kRing + 4 * kItemRing;
+  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, -, wait limit
+  static constexpr int kRing = kMisc + 16;                    // [kItemRing] x {key tile, batch-head, key length, -}
+  static constexpr int kSmemBytes = kRing + 16 * kItemRing;
+  // the dQ partial is drained per warp (each warp adds its own 32 rows) at
+  // d = 128 and by the four warps together (whole 128-row boxes) at d = 64:
+  // measured, each is the faster one at its width
+  static constexpr bool kGroupDrain = (D == 64);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -130,7 +134,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // within a group, low key tiles (the most live query tiles) first. A CTA
   // starts with item blockIdx.x and then takes the next unclaimed one from a
   // grid-wide counter (zeroed by the pre-pass), so that items are handed out
-  // in order, each to the first CTA that is ready for one.
+  // in order, each to the first CTA that is ready for one. The producer
+  // decodes each item once and hands it to the other roles through the ring.
   const int total = p.nT * BH;
   struct Item {
     int kj, bh, kvl;   // key tile, batch-head, key length of the batch entry
@@ -150,27 +155,28 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     while (i < p.nT && tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kSkip) ++i;
     return i;
   };
-  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
+  Ctl ctl{p.err, abort_flag};
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
-  // item k of this CTA from the ring; -1 when none is left or a wait failed
-  auto take_item = [&](int k, bool warp_wide, bool& ok) -> int {
+  // item k of this CTA from the ring; kj < 0 when none is left or a wait
+  // failed (then ok is false too)
+  auto take_item = [&](int k, bool warp_wide, bool& ok) -> Item {
     const int rs = k % L::kItemRing;
     const uint32_t ph = (uint32_t)(k / L::kItemRing) & 1u;
     ok = warp_wide ? mbar_wait_warp(bar(L::bItemFull + rs), ph, ctl, 105)
                    : mbar_wait(bar(L::bItemFull + rs), ph, ctl, 105);
-    if (!ok) return -1;
-    const int item = ring[rs];
+    if (!ok) return Item{-1, 0, 0};
+    const Item w{ring[4 * rs], ring[4 * rs + 1], ring[4 * rs + 2]};
     if (warp_wide)
       mbar_arrive_warp(bar(L::bItemEmpty + rs));
     else
       mbar_arrive(bar(L::bItemEmpty + rs));
-    return item;
+    return w;
   };
 
   if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
     if (tid == 0) {
-      uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy, p.chk.wait_ns};
+      uint32_t dummy = 0;   // report_error writes only the abort flag
+      Ctl c0{p.err, &dummy};
       report_error(c0, kErrSmemAlign, 100);
     }
     return;
@@ -181,8 +187,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull) ? 8u
                         : i == L::bdQFree ? 4u                                       // the four drain warps
                         : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 2u         // one thread per compute group
+                        : (!L::kGroupDrain && i >= L::bdOFree && i < L::bdOFree + L::kStages) ? 4u   // the drain warps
                         : i >= L::bItemEmpty ? 13u : 1u);   // arrivals
-    *abort_flag = 0u;
+    abort_flag[0] = 0u;
+    abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -251,10 +259,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             !(ok = mbar_wait(bar(L::bItemEmpty + rs), (uint32_t)(k / L::kItemRing - 1) & 1u, ctl, 104)))
           break;
         const int item = k == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(p.sched, 1u);
-        ring[rs] = item < total ? item : -1;
-        mbar_arrive(bar(L::bItemFull + rs));
-        if (item >= total) break;
-        const Item w = item_at(item);
+        const bool more = item < total;
+        const Item w = more ? item_at(item) : Item{-1, 0, 0};
+        ring[4 * rs] = w.kj;
+        ring[4 * rs + 1] = w.bh;
+        ring[4 * rs + 2] = w.kvl;
+        mbar_arrive(bar(L::bItemFull + rs));   // (release: the ring entry is visible to the waiters)
+        if (!more) break;
         int i = next_live(w, 0);
         if (i >= p.nT) {
           ok = load_kv(k, w, false);
@@ -317,9 +328,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int item = take_item(k, false, ok);
-        if (item < 0) break;
-        const Item w = item_at(item);
+        const Item w = take_item(k, false, ok);
+        if (w.kj < 0) break;
         int i = next_live(w, 0);
         if (i >= p.nT) continue;
         const int kb = k % L::kKV;
@@ -408,10 +418,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     // all of them take the same branch and none waits for one that has left.
     const uint32_t gbar = 1u + (uint32_t)cw;
     for (int k = 0; ok; ++k) {
-      const int item = take_item(k, true, ok);
+      const Item w = take_item(k, true, ok);
       ok = group_all(gbar, 128, ok);
-      if (!ok || item < 0) break;
-      const Item w = item_at(item);
+      if (!ok || w.kj < 0) break;
       const int krow = kTile * w.kj + r;
       int i = next_live(w, 0);
       const bool live = i < p.nT;
@@ -421,10 +430,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 120))) break;
         if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 121))) break;
         tc_fence_after();
-        if (p.chk.rec != nullptr && tid == 0) {   // the tile as this kernel computes it
-          uint8_t* rc = p.chk.rec + ((size_t)w.bh * p.nT + i) * p.nT + w.kj;
-          *rc = (uint8_t)(*rc + (partial ? 2 : 1));
-        }
+        if (p.chk.rec != nullptr && tid == 0) record_tile(p.chk.rec, w.bh, i, w.kj, p.nT, partial);   // as computed
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
         const float* dlt = lse2 + kTile;
         float x[64];
@@ -588,31 +594,35 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
-    // has completed) in two rounds of boxes of [128 rows x 32 fp32], 128-byte
-    // swizzled -> TMA reduce-add into the accumulator. The TMEM columns are
-    // released as soon as they are all in registers or staged; the slot goes
-    // back to the producer when the last round has been read. The four warps
-    // meet at named barriers in every round; after each wait that one of them
-    // may fail they agree with group_all, so that they always take the same
-    // branch.
+    // has completed) in two rounds of 32-column boxes, 128-byte swizzled ->
+    // TMA reduce-add into the accumulator. The TMEM columns are released as
+    // soon as they are all in registers or staged; the slot goes back to the
+    // producer when its last round has been read.
+    //   d = 128: each warp stages and adds its own 32 query rows (boxes of 32
+    //            rows) and synchronises only within itself.
+    //   d = 64:  the four warps stage whole 128-row boxes that one thread adds,
+    //            meeting at named barriers; after each wait that one of them
+    //            may fail they agree with group_all, so that they always take
+    //            the same branch and none waits at a barrier another has left.
     regs_dec<kDrainRegs>();
     constexpr int kBoxesPerRound = L::kTileBytes / 16384;    // 1 (d = 64) or 2 (d = 128)
     constexpr int kRounds = D / 32 / kBoxesPerRound;
     const int r = tid - 256;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+    const uint32_t wrow = L::kGroupDrain ? 0u : 4096u * (uint32_t)(warp & 3);   // this warp's rows in a box
     bool ok = true;
     int g = 0;
     for (int k = 0; ok; ++k) {
-      const int item = take_item(k, true, ok);
-      ok = group_all(3, 128, ok);
-      if (!ok || item < 0) break;
-      const Item w = item_at(item);
+      const Item w = take_item(k, true, ok);
+      if constexpr (L::kGroupDrain) ok = group_all(3, 128, ok);
+      if (!ok || w.kj < 0) break;
       for (int i = next_live(w, 0); i < p.nT; ++g, i = next_live(w, i + 1)) {
         const int s = g % L::kStages;
         const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
         ok = mbar_wait_warp(bar(L::bdQFull), (uint32_t)g & 1u, ctl, 130);
-        if (!(ok = group_all(3, 128, ok))) break;
+        if constexpr (L::kGroupDrain) ok = group_all(3, 128, ok);
+        if (!ok) break;
         tc_fence_after();
         uint32_t u[kBoxesPerRound][32];
 #pragma unroll
@@ -626,8 +636,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_arrive_warp(bar(L::bdQFree));   // every dQ column is in registers or staged
           }
           if (round > 0) {              // the previous round has been read out of the slot
-            if (r == 0) bulk_wait_group_read_all();
-            named_bar_sync(3, 128);
+            if constexpr (L::kGroupDrain) {
+              if (r == 0) bulk_wait_group_read_all();
+              named_bar_sync(3, 128);
+            } else {
+              if (lane == 0) bulk_wait_group_read_all();
+              __syncwarp();
+            }
           }
 #pragma unroll
           for (int b = 0; b < kBoxesPerRound; ++b)
@@ -638,13 +653,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                   make_uint4(u[b][4 * k8], u[b][4 * k8 + 1], u[b][4 * k8 + 2], u[b][4 * k8 + 3]);
             }
           fence_proxy_async_smem();
-          named_bar_sync(3, 128);
-          if (r == 0) {
+          if constexpr (L::kGroupDrain)
+            named_bar_sync(3, 128);
+          else
+            __syncwarp();
+          if (L::kGroupDrain ? r == 0 : lane == 0) {
+            const int row0 = kTile * i + (L::kGroupDrain ? 0 : 32 * (warp & 3));
 #pragma unroll
             for (int b = 0; b < kBoxesPerRound; ++b)
               if (32 * (round * kBoxesPerRound + b) < p.d)   // boxes wholly past the head dimension hold zeros
-                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b, 32 * (round * kBoxesPerRound + b),
-                                  kTile * i, w.bh);
+                tma_reduce_add_3d(&tdq, sbase + stage + 16384u * b + wrow, 32 * (round * kBoxesPerRound + b),
+                                  row0, w.bh);
             bulk_commit_group();
           }
           if (round + 1 < kRounds) {    // the next columns into registers while the round is read
@@ -655,13 +674,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int b = 0; b < kBoxesPerRound; ++b) tmem_ld_wait(u[b]);
           }
         }
-        if (r == 0) {
+        if (L::kGroupDrain ? r == 0 : lane == 0) {
           bulk_wait_group_read_all();
           mbar_arrive(bar(L::bdOFree + s));
         }
       }
     }
-    if (r == 0) bulk_wait_group_all();     // reductions complete before exit
+    if (L::kGroupDrain ? r == 0 : lane == 0) bulk_wait_group_all();     // reductions complete before exit
   }
 
   tc_fence_before();

@@ -58,12 +58,12 @@ struct DropoutParams {
 // uint8 [BH, nT, nT] record of the tiles a kernel computed: the thread that
 // decides whether a tile needs element masking adds 1 (no masking) or 2
 // (masking) to the tile's byte, so that a tile computed twice would show as a
-// larger value. wait_ns bounds every mbarrier wait. stall (test only, 0 in
+// larger value. wait_us bounds every mbarrier wait. stall (test only, 0 in
 // normal use) makes a producer stop loading after its first tile, so that a
 // consumer's bounded wait runs out and the kernel reports a timeout.
 struct CheckParams {
   uint8_t* rec;
-  unsigned long long wait_ns;
+  uint32_t wait_us;
   uint32_t stall;
 };
 
@@ -97,6 +97,14 @@ struct BwdParams {
   int d;                      // head dimension of the tensors (<= the kernel's tile width)
   int group;                  // heads per group of the work-item order (set by the launcher)
 };
+
+// Adds 1 (no element mask) or 2 (masked) to the record byte of tile (qi, kj)
+// of batch-head bh. Out of line: it runs only when a caller asks for the
+// record, and keeps its address arithmetic out of the hot loops' registers.
+__device__ __noinline__ inline void record_tile(uint8_t* rec, int bh, int qi, int kj, int nT, bool partial) {
+  uint8_t* rc = rec + ((size_t)bh * nT + qi) * nT + kj;
+  *rc = (uint8_t)(*rc + (partial ? 2 : 1));
+}
 
 // Heads per group when the work of a launch is ordered group by group so that
 // the data one group touches stays in L2 (~126 MB): bytes_per_head is what a

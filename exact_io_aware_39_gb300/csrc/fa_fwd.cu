@@ -69,7 +69,7 @@ struct FwdLayout {
   static constexpr int bOFinal = bPFull + 2;          // [2]
   static constexpr int bDrain = bOFinal + 2;
   static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort, list length
+  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, list length, wait limit
   static constexpr int kList = kMisc + 16;           // uint16 entries
   static constexpr int kSmemBytes = kList + 2 * kListMax;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -108,12 +108,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
-  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
+  Ctl ctl{p.err, abort_flag};
 
   if ((sbase & 1023u) != 0u) {   // uniform across the CTA: nothing has started yet
     if (tid == 0) {
-      uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy, p.chk.wait_ns};
+      uint32_t dummy = 0;   // report_error writes only the abort flag
+      Ctl c0{p.err, &dummy};
       report_error(c0, kErrSmemAlign, 0);
     }
     return;
@@ -122,7 +122,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
       mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 4u : 1u);   // 4 = warps
-    *abort_flag = 0u;
+    abort_flag[0] = 0u;
+    abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
   }
   if (warp == 9) {

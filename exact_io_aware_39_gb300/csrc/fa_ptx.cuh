@@ -21,10 +21,11 @@ namespace fa {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: default bound of a wait, and of every drain wait
 
+// The wait limit is kept in shared memory next to the abort flag (read only
+// on the slow path of a wait), so that it holds no register in the roles.
 struct Ctl {
   unsigned int* err;          // global error word (4 x u32)
-  volatile uint32_t* abort;   // shared abort flag of this CTA
-  uint64_t limit;             // bound of one mbarrier wait, ns
+  volatile uint32_t* abort;   // [0] abort flag of this CTA, [2] bound of one mbarrier wait in microseconds
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -141,7 +142,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const C
     if (mbar_try(bar, parity)) return true;
     if ((++n & 15u) == 0u) {
       if (*c.abort) return false;
-      if (globaltimer() - t0 > c.limit) {
+      if (globaltimer() - t0 > 1000ull * c.abort[2]) {
         report_error(c, kErrTimeout, site);
         return false;
       }

@@ -69,7 +69,7 @@ struct WFwdLayout {
   static constexpr int bOFinal = bPV + 2;
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kMisc = kBar + 8 * kNumBars;    // tmem slot, abort, list length
+  static constexpr int kMisc = kBar + 8 * kNumBars;    // tmem slot, abort flag, list length, wait limit
   static constexpr int kList = kMisc + 16;             // uint16 entries
   static constexpr int kSmemBytes = kList + 2 * kWListMax;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -102,19 +102,20 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::kList);
-  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
+  Ctl ctl{p.err, abort_flag};
 
   if ((sbase & 1023u) != 0u) {
     if (tid == 0) {
-      uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy, p.chk.wait_ns};
+      uint32_t dummy = 0;   // report_error writes only the abort flag
+      Ctl c0{p.err, &dummy};
       report_error(c0, kErrSmemAlign, 40);
     }
     return;
   }
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 4u : 1u);
-    *abort_flag = 0u;
+    abort_flag[0] = 0u;
+    abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -250,10 +251,8 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const uint32_t tSe = tmem + 128u * (uint32_t)(e & 1) + lane_off;
       if (!(ok = mbar_wait_warp(bar(L::bSFull + (e & 1)), (uint32_t)(e >> 1) & 1u, ctl, 50))) break;
       tc_fence_after();
-      if (p.chk.rec != nullptr && r == 0) {   // the tile as this kernel computes it
-        uint8_t* rc = p.chk.rec + ((size_t)bh * p.nT + qi) * p.nT + wentry_j(ent);
-        *rc = (uint8_t)(*rc + (wentry_partial(ent) ? 2 : 1));
-      }
+      if (p.chk.rec != nullptr && r == 0)   // the tile as this kernel computes it
+        record_tile(p.chk.rec, bh, qi, wentry_j(ent), p.nT, wentry_partial(ent));
       float x[128];
       {
         uint32_t u0[32], u1[32], u2[32], u3[32];
@@ -431,7 +430,7 @@ struct WBwdLayout {
   static constexpr int bItemFull = 15;                       // [kItemRing]
   static constexpr int bItemEmpty = bItemFull + kItemRing;   // [kItemRing], 13 arrivals
   static constexpr int kNumBars = bItemEmpty + kItemRing;
-  static constexpr int kMisc = kBar + 8 * kNumBars;
+  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, -, wait limit
   static constexpr int kRing = kMisc + 16;
   static constexpr int kSmemBytes = kRing + 4 * kItemRing;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -487,7 +486,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile uint32_t* abort_flag = misc + 1;
-  Ctl ctl{p.err, abort_flag, p.chk.wait_ns};
+  Ctl ctl{p.err, abort_flag};
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   auto take_item = [&](int k, bool warp_wide, bool& ok) -> int {
     const int rs = k % L::kItemRing;
@@ -505,8 +504,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if ((sbase & 1023u) != 0u) {
     if (tid == 0) {
-      uint32_t dummy = 0;
-      Ctl c0{p.err, &dummy, p.chk.wait_ns};
+      uint32_t dummy = 0;   // report_error writes only the abort flag
+      Ctl c0{p.err, &dummy};
       report_error(c0, kErrSmemAlign, 150);
     }
     return;
@@ -516,7 +515,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bKVFree) ? 8u
                         : i == L::bdQFree ? 4u
                         : i >= L::bItemEmpty ? 13u : 1u);
-    *abort_flag = 0u;
+    abort_flag[0] = 0u;
+    abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
   }
   if (warp == 13) {
@@ -672,10 +672,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = mbar_wait_warp(bar(L::bQFull), (uint32_t)g & 1u, ctl, 170))) break;
         if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 171))) break;
         tc_fence_after();
-        if (p.chk.rec != nullptr && tid == 0 && w.hd == 0 && sub == 0) {   // the tile as this kernel computes it
-          uint8_t* rc = p.chk.rec + ((size_t)w.bh * p.nT + i) * p.nT + w.kj;
-          *rc = (uint8_t)(*rc + (partial ? 2 : 1));
-        }
+        if (p.chk.rec != nullptr && tid == 0 && w.hd == 0 && sub == 0)   // the tile as this kernel computes it
+          record_tile(p.chk.rec, w.bh, i, w.kj, p.nT, partial);
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow) + cb;
         const float* dlt = lse2 + 64;
         float x[32];
