@@ -790,7 +790,7 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
-  return launch_pdl(fa_bwd_main_kernel<D, F16, DROP>, grid, dim3(kBwdThreads), L::kSmemBytes, s, tq, tk, tv, tdo,
+  return launch_pdl(true, fa_bwd_main_kernel<D, F16, DROP>, grid, dim3(kBwdThreads), L::kSmemBytes, s, tq, tk, tv, tdo,
                     tdk, tdv, tdq, q, scale);
 }
 
@@ -808,7 +808,7 @@ cudaError_t launch_bwd_pre(bool f16, const void* o, const void* dout, const floa
   const uint16_t* g16 = static_cast<const uint16_t*>(dout);
 #define FA_PRE_CASE(GG)                                                                                       \
   if (G == GG)                                                                                                \
-    return launch_pdl(f16 ? fa_bwd_pre_kernel<GG, true> : fa_bwd_pre_kernel<GG, false>, dim3(grid), dim3(block), 0, \
+    return launch_pdl(false, f16 ? fa_bwd_pre_kernel<GG, true> : fa_bwd_pre_kernel<GG, false>, dim3(grid), dim3(block), 0, \
                       s, o16, g16, lse, dq_acc, lse2, delta, sched, BH, N, Np, d);
   FA_PRE_CASE(1)
   FA_PRE_CASE(2)
@@ -849,7 +849,7 @@ cudaError_t launch_bwd_dq(bool f16, const float* dq_acc, void* dq, float scale, 
   const long long threads = (long long)BH * N * (d / 8);
   const int block = 256;
   const unsigned grid = (unsigned)((threads + block - 1) / block);
-  return launch_pdl(f16 ? fa_bwd_dq_kernel<true> : fa_bwd_dq_kernel<false>, dim3(grid), dim3(block), 0, s, dq_acc,
+  return launch_pdl(false, f16 ? fa_bwd_dq_kernel<true> : fa_bwd_dq_kernel<false>, dim3(grid), dim3(block), 0, s, dq_acc,
                     static_cast<uint16_t*>(dq), scale, BH, N, Np, d);
 }
 

@@ -503,7 +503,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const int nC = (p.nT + 1) / 2;
   const dim3 grid((unsigned)(nC * p.B * p.H));
-  return launch_pdl(fa_fwd_kernel<D, F16, DROP>, grid, dim3(kFwdThreads), L::kSmemBytes, s, tq, tk, tv, to, q);
+  return launch_pdl(true, fa_fwd_kernel<D, F16, DROP>, grid, dim3(kFwdThreads), L::kSmemBytes, s, tq, tk, tv, to, q);
 }
 
 }  // namespace

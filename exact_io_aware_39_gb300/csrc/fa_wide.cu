@@ -862,7 +862,7 @@ cudaError_t launch_fwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& 
   FwdParams q = p;
   q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  return launch_pdl(kern, grid, dim3(kWFwdThreads), WFwdLayout::kSmemBytes, s, tq, tk, tv, to, q);
+  return launch_pdl(true, kern, grid, dim3(kWFwdThreads), WFwdLayout::kSmemBytes, s, tq, tk, tv, to, q);
 }
 
 cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -884,7 +884,7 @@ cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& 
   const long long items = 2LL * p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
   const float scale = p.scale_log2 / 1.4426950408889634f;
-  return launch_pdl(kern, grid, dim3(kWBwdThreads), WBwdLayout::kSmemBytes, s, tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
+  return launch_pdl(true, kern, grid, dim3(kWBwdThreads), WBwdLayout::kSmemBytes, s, tq, tk, tv, tdo, tdk, tdv, tdq, q, scale);
 }
 
 }  // namespace fa
