@@ -538,12 +538,14 @@ def run_ours(args):
     fwd_avg = statistics.mean(fwd_ms)
     achieved = f_bwd / (bwd_avg * 1e-3) / 1e12
     tr = _traffic_record(f"bwd_main:{w.name}")
+    trf = _traffic_record(f"fwd:{w.name}")
     roofline = {"kernel": "fa_bwd_main_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"{'sustained' if peak == peak_sust else 'burst'} bf16, {peak_src}",
                 "traffic": None if tr is None else tr["dram_bytes_per_launch"],
                 "fwd_kernel": {"achieved": f_fwd / (fwd_avg * 1e-3) / 1e12,
-                               "frac": f_fwd / (fwd_avg * 1e-3) / 1e12 / peak, "ms": fwd_avg},
+                               "frac": f_fwd / (fwd_avg * 1e-3) / 1e12 / peak, "ms": fwd_avg,
+                               "traffic": None if trf is None else trf["dram_bytes_per_launch"]},
                 "bwd_main_ms": bwd_avg,
                 "kernel_times": "CUDA events around each kernel on its stream, in a second pass of the same "
                                 "K steps right after the timed one"}

@@ -463,20 +463,30 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         // dropout: keep bits of this warpgroup's 64 query columns; one generator
         // call (counter (query / 4, key / 4, bh, 0)) covers 4 queries, byte
-        // key mod 4 of each of its 4 words
+        // key mod 4 of each of its 4 words. The four key rows of a lane quad
+        // share their calls: each lane makes the call of one 4-query block,
+        // turns its 16 bytes into 16 keep bits (bit 4 j + k: query j, key k of
+        // the block) and the quad passes the masks around (4 calls per row and
+        // tile instead of 16)
         uint32_t keep[2] = {0u, 0u};
         if constexpr (DROP) {
           const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
-          const uint32_t sh = 8u * ((uint32_t)krow & 3u);
+          const uint32_t s4 = (uint32_t)lane & 3u;   // = key row mod 4
+          const uint32_t t4 = p.drop.t * 0x01010101u;
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const uint4 v = philox4x32_10(qb0 + (uint32_t)m, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
+          for (int m4 = 0; m4 < 4; ++m4) {
+            const uint4 v = philox4x32_10(qb0 + 4u * (uint32_t)m4 + s4, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
                                           p.drop.seed_lo, p.drop.seed_hi);
-            const uint32_t bits = (((v.x >> sh) & 0xFFu) >= p.drop.t ? 1u : 0u) |
-                                  (((v.y >> sh) & 0xFFu) >= p.drop.t ? 2u : 0u) |
-                                  (((v.z >> sh) & 0xFFu) >= p.drop.t ? 4u : 0u) |
-                                  (((v.w >> sh) & 0xFFu) >= p.drop.t ? 8u : 0u);
-            keep[m >> 3] |= bits << (4 * (m & 7));
+            const uint32_t m16 = bytes_ge_nibble(v.x, t4) | (bytes_ge_nibble(v.y, t4) << 4) |
+                                 (bytes_ge_nibble(v.z, t4) << 8) | (bytes_ge_nibble(v.w, t4) << 12);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t mu = __shfl_sync(0xFFFFFFFFu, m16, (lane & ~3) | u);   // query block 4 m4 + u
+              const uint32_t b = (mu >> s4) & 0x1111u;
+              const uint32_t bits = (b | (b >> 3) | (b >> 6) | (b >> 9)) & 0xFu;   // queries 0..3 of the block
+              const int m = 4 * m4 + u;
+              keep[m >> 3] |= bits << (4 * (m & 7));
+            }
           }
         }
         auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };

@@ -386,9 +386,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       const float2 nref2 = make_float2(-ref, -ref);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
-      // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4
+      // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
+      // four rows of a lane quad share their calls: for every 16 keys each
+      // lane makes the call of one 4-key block and a transpose across the
+      // quad hands every row its word of all four (one call per 16 keys and
+      // row instead of four)
       const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
-      uint32_t rw = 0;
+      uint32_t kw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
@@ -399,10 +403,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           const float p1 = ex2(a.y);
           sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
           if constexpr (DROP) {
-            if ((i & 1) == 0)
-              rw = uint4_word(philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1),
-                                            (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi),
-                              (uint32_t)row & 3u);
+            if ((i & 7) == 0) {
+              const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
+                                            (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
+              kw[0] = v.x;
+              kw[1] = v.y;
+              kw[2] = v.z;
+              kw[3] = v.w;
+              quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
+            }
+            const uint32_t rw = kw[(i >> 1) & 3];
             const uint32_t sh = 16u * (uint32_t)(i & 1);
             const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
             const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;

@@ -485,6 +485,36 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(c0, c1, c2, c3);
 }
 
+// 4 x 4 transpose of 32-bit words across the four lanes of a lane quad (lane
+// index s = lane mod 4): lane s holds x[j] = M[s][j] on entry and
+// x[j] = M[j][s] on exit. Two butterfly rounds (lane distance 1, then 2), in
+// each of which a lane swaps the two words whose index differs from its own in
+// that bit. Every lane of the warp must take part.
+__device__ __forceinline__ void quad_transpose(uint32_t (&x)[4], uint32_t s) {
+  const bool h1 = (s & 1u) != 0u;
+  uint32_t v0 = h1 ? x[0] : x[1], v1 = h1 ? x[2] : x[3];
+  v0 = __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+  v1 = __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+  if (h1) { x[0] = v0; x[2] = v1; } else { x[1] = v0; x[3] = v1; }
+  const bool h2 = (s & 2u) != 0u;
+  v0 = h2 ? x[0] : x[2];
+  v1 = h2 ? x[1] : x[3];
+  v0 = __shfl_xor_sync(0xFFFFFFFFu, v0, 2);
+  v1 = __shfl_xor_sync(0xFFFFFFFFu, v1, 2);
+  if (h2) { x[0] = v0; x[1] = v1; } else { x[2] = v0; x[3] = v1; }
+}
+
+// Bit k (k = 0..3) set when byte k of w is >= the byte of t4 (t4 = t repeated
+// in all four bytes), unsigned. Bytewise a >= b is "a - b does not borrow":
+// with the top bits set aside, (a | 0x80..) - (b & 0x7F..) leaves in bit 7 of
+// each byte whether the low 7 bits of a are >= those of b; the top bits then
+// decide where a and b differ there.
+__device__ __forceinline__ uint32_t bytes_ge_nibble(uint32_t w, uint32_t t4) {
+  const uint32_t d = (w | 0x80808080u) - (t4 & 0x7F7F7F7Fu);
+  const uint32_t g = ((w & ~t4) | (~(w ^ t4) & d)) & 0x80808080u;
+  return ((g >> 7) | (g >> 14) | (g >> 21) | (g >> 28)) & 0xFu;
+}
+
 __device__ __forceinline__ uint32_t uint4_word(const uint4& v, uint32_t i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
