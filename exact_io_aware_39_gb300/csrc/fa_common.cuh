@@ -206,8 +206,10 @@ cudaError_t launch_bwd_main(int d, bool f16, const CUtensorMap& tq, const CUtens
 
 // The kernels for 128 < d <= 256 (fa_wide.cu; no dropout). The backward's
 // tq and tdo are views with 64-row boxes (queries are taken 64 at a time).
-cudaError_t launch_fwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
+// The one-Q-tile forward (S double-buffered in TMEM, K/V streamed in units of
+// up to 128 columns) for a kernel head dimension kd of 64, 128 or 256.
+cudaError_t launch_fwd_single(int kd, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, const FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                             const CUtensorMap& tdq, const BwdParams& p, cudaStream_t s);

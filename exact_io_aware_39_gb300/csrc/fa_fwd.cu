@@ -522,7 +522,7 @@ cudaError_t launch_fwd(int d, bool f16, const CUtensorMap& tq, const CUtensorMap
                        const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   const bool drop = p.drop.t > 0;
   const int kd = kernel_head_dim(d);
-  if (kd == 256) return drop ? cudaErrorInvalidValue : launch_fwd_wide(f16, tq, tk, tv, to, p, s);
+  if (kd == 256) return drop ? cudaErrorInvalidValue : launch_fwd_single(kd, f16, tq, tk, tv, to, p, s);
 #define FA_FWD_CASE(DD, FF, DR) \
   if (kd == DD && f16 == FF && drop == DR) return launch_fwd_d<DD, FF, DR>(tq, tk, tv, to, p, s);
   FA_FWD_CASE(64, false, false)

@@ -9,9 +9,11 @@
 // width d fills half of the 512 TMEM columns, so both kernels are laid out
 // differently from the narrower ones:
 //
-// Forward (fa_fwd_wide_kernel): one 128-row Q tile per CTA (64 KB, resident);
-// K and V stream through a ring of five 32 KB half tiles (128 keys x 128
-// columns) in the order the tensor core reads them. TMEM: S twice (2 x 128
+// Forward (fa_fwd_wide_kernel<256>): one 128-row Q tile per CTA (64 KB,
+// resident); K and V stream through a ring of five 32 KB half tiles (128 keys
+// x 128 columns) in the order the tensor core reads them (the kernel is
+// written for any tile width of 64, 128 or 256 columns, in ring units of up to
+// 128 columns). TMEM: S twice (2 x 128
 // fp32 columns, so that S of the next key tile is computed while the softmax
 // works on this one) and O (256 columns). Schedule of the single MMA thread:
 //   S(0), S(1), PV(0), S(2), PV(1), ...   (PV(e) once P(e) is in TMEM)
@@ -54,12 +56,19 @@ constexpr float kWRescaleThreshold = 8.0f;   // log2 units, as in the narrow for
 // forward
 // --------------------------------------------------------------------------
 
+// Layout of the one-Q-tile forward for a tile width D (64, 128 or 256): K and
+// V stream through a ring of units of 128 keys x U columns (U = min(D, 128)),
+// D / U units per tile, in the order the MMA thread reads them.
+template <int D>
 struct WFwdLayout {
-  static constexpr int kHalfBytes = kTile * 128 * 2;   // 128 rows x 128 columns, 16-bit: 32 KB
-  static constexpr int kSlots = 5;
-  static constexpr int kQ = 0;                         // 128 x 256: four 16 KB atoms
-  static constexpr int kRing = kQ + 4 * 16384;         // [kSlots] half tiles, two atoms each
-  static constexpr int kBar = kRing + kSlots * kHalfBytes;
+  static constexpr int kU = D < 128 ? D : 128;          // columns per ring unit
+  static constexpr int kUnits = D / kU;                  // units per K or V tile
+  static constexpr int kAtomsPerUnit = kU / 64;
+  static constexpr int kUnitBytes = kTile * kU * 2;
+  static constexpr int kSlots = D == 64 ? 12 : (D == 128 ? 6 : 5);
+  static constexpr int kQ = 0;                           // 128 x D: D / 64 atoms of 16 KB
+  static constexpr int kRing = kQ + (D / 64) * 16384;    // [kSlots] units
+  static constexpr int kBar = kRing + kSlots * kUnitBytes;
   static constexpr int bQFull = 0;
   static constexpr int bFull = 1;                      // [kSlots]
   static constexpr int bEmpty = bFull + kSlots;        // [kSlots]
@@ -81,12 +90,12 @@ constexpr int kWFwdThreads = 192;
 __device__ __forceinline__ int wentry_j(uint32_t e) { return (int)(e & 0x3FFu); }
 __device__ __forceinline__ bool wentry_partial(uint32_t e) { return (e >> 10) & 1u; }
 
-template <bool F16>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kWFwdThreads, 1)
 fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                    const FwdParams p) {
-  using L = WFwdLayout;
+  using L = WFwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x;
@@ -150,31 +159,31 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tma_prefetch_map(&tq);
       tma_prefetch_map(&tk);
       tma_prefetch_map(&tv);
-      mbar_arrive_expect_tx(bar(L::bQFull), 4u * 16384u);
-      for (int a = 0; a < 4; ++a) tma_load_3d(sbase + L::kQ + a * 16384, &tq, bar(L::bQFull), 64 * a, kTile * qi, bh);
-      int u = 0;   // half tiles issued, in the order the MMA thread reads them: K(0), then K(e+1), V(e) per entry
-      auto load_half = [&](const CUtensorMap* m, int j, int half) -> bool {
+      mbar_arrive_expect_tx(bar(L::bQFull), (uint32_t)(D / 64) * 16384u);
+      for (int a = 0; a < D / 64; ++a) tma_load_3d(sbase + L::kQ + a * 16384, &tq, bar(L::bQFull), 64 * a, kTile * qi, bh);
+      int u = 0;   // units issued, in the order the MMA thread reads them: K(0), then K(e+1), V(e) per entry
+      auto load_unit = [&](const CUtensorMap* m, int j, int unit) -> bool {
         const int s = u % L::kSlots;
         const uint32_t n = (uint32_t)(u / L::kSlots);
         if (u >= L::kSlots && !mbar_wait(bar(L::bEmpty + s), (n - 1) & 1u, ctl, 41)) return false;
-        mbar_arrive_expect_tx(bar(L::bFull + s), (uint32_t)L::kHalfBytes);
-        for (int a = 0; a < 2; ++a)
-          tma_load_3d(sbase + L::kRing + s * L::kHalfBytes + a * 16384, m, bar(L::bFull + s), 128 * half + 64 * a,
+        mbar_arrive_expect_tx(bar(L::bFull + s), (uint32_t)L::kUnitBytes);
+        for (int a = 0; a < L::kAtomsPerUnit; ++a)
+          tma_load_3d(sbase + L::kRing + s * L::kUnitBytes + a * 16384, m, bar(L::bFull + s), L::kU * unit + 64 * a,
                       kTile * j, bh);
         ++u;
         return true;
       };
+      auto load_tile = [&](const CUtensorMap* m, int j) -> bool {
+        for (int unit = 0; unit < L::kUnits; ++unit)
+          if (!load_unit(m, j, unit)) return false;
+        return true;
+      };
       if (len > 0) {
-        const int j0 = wentry_j(list[0]);
-        bool ok = load_half(&tk, j0, 0) && load_half(&tk, j0, 1);
+        bool ok = load_tile(&tk, wentry_j(list[0]));
         for (int e = 0; e < len && ok; ++e) {
           if (p.chk.stall != 0u) break;   // test of the timeout path: nothing after K of entry 0
-          if (e + 1 < len) {
-            const int j1 = wentry_j(list[e + 1]);
-            if (!(ok = load_half(&tk, j1, 0) && load_half(&tk, j1, 1))) break;
-          }
-          const int j = wentry_j(list[e]);
-          ok = load_half(&tv, j, 0) && load_half(&tv, j, 1);
+          if (e + 1 < len && !(ok = load_tile(&tk, wentry_j(list[e + 1])))) break;
+          ok = load_tile(&tv, wentry_j(list[e]));
         }
       }
       drain_wait(bar(L::bQFull), 0);
@@ -185,45 +194,50 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
-      constexpr uint32_t idO = idesc_16<F16>(128, 128, false, true);
+      constexpr uint32_t idO = idesc_16<F16>(128, L::kU, false, true);
+      constexpr int kStepsPerUnit = L::kU / 16;
       const uint32_t tS[2] = {tmem, tmem + 128u};
       const uint32_t tO = tmem + 256u;
       const uint64_t dQ0 = desc_kmajor(sbase + L::kQ, 0);
       bool ok = mbar_wait(bar(L::bQFull), 0, ctl, 44);
       tc_fence_after();
       int u = 0;
-      auto slot = [&](int uu) -> uint32_t { return sbase + L::kRing + (uint32_t)(uu % L::kSlots) * L::kHalfBytes; };
-      auto wait_slot = [&](int uu, uint32_t site) -> bool {
-        return mbar_wait(bar(L::bFull + uu % L::kSlots), (uint32_t)(uu / L::kSlots) & 1u, ctl, site);
-      };
-      // S(e) = Q K_e^T into buffer e mod 2 (K in half tiles u, u + 1)
-      auto issue_s = [&](int e) -> bool {
-        if (!wait_slot(u, 45) || !wait_slot(u + 1, 45)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks)
-          mma_ss(tS[e & 1], dQ0 + kmajor_step(ks), desc_kmajor(slot(u + (ks >> 3)), ks & 7), idS, ks > 0 ? 1u : 0u);
-        mma_commit(bar(L::bEmpty + u % L::kSlots));
-        mma_commit(bar(L::bEmpty + (u + 1) % L::kSlots));
-        mma_commit(bar(L::bSFull + (e & 1)));
-        u += 2;
+      auto slot = [&](int uu) -> uint32_t { return sbase + L::kRing + (uint32_t)(uu % L::kSlots) * L::kUnitBytes; };
+      auto wait_units = [&](uint32_t site) -> bool {
+        for (int unit = 0; unit < L::kUnits; ++unit)
+          if (!mbar_wait(bar(L::bFull + (u + unit) % L::kSlots), (uint32_t)((u + unit) / L::kSlots) & 1u, ctl, site))
+            return false;
         return true;
       };
-      // O += P(e) V_e (V in half tiles u, u + 1: output columns 0-127, 128-255)
-      auto issue_pv = [&](int e) -> bool {
-        if (!mbar_wait(bar(L::bPFull + (e & 1)), (uint32_t)(e >> 1) & 1u, ctl, 46)) return false;
-        if (!wait_slot(u, 47) || !wait_slot(u + 1, 47)) return false;
+      auto release_units = [&]() {
+        for (int unit = 0; unit < L::kUnits; ++unit) mma_commit(bar(L::bEmpty + (u + unit) % L::kSlots));
+        u += L::kUnits;
+      };
+      // S(e) = Q K_e^T into buffer e mod 2 (K in units u ..)
+      auto issue_s = [&](int e) -> bool {
+        if (!wait_units(45)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tS[e & 1], dQ0 + kmajor_step(ks), desc_kmajor(slot(u + ks / kStepsPerUnit), ks % kStepsPerUnit), idS,
+                 ks > 0 ? 1u : 0u);
+        release_units();
+        mma_commit(bar(L::bSFull + (e & 1)));
+        return true;
+      };
+      // O += P(e) V_e (V in units u ..: output columns kU h .. kU h + kU - 1)
+      auto issue_pv = [&](int e) -> bool {
+        if (!mbar_wait(bar(L::bPFull + (e & 1)), (uint32_t)(e >> 1) & 1u, ctl, 46)) return false;
+        if (!wait_units(47)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < L::kUnits; ++h)
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ts(tO + 128u * h, tS[e & 1] + (uint32_t)ks * 8u, desc_mnmajor(slot(u + h), ks), idO,
+            mma_ts(tO + (uint32_t)(L::kU * h), tS[e & 1] + (uint32_t)ks * 8u, desc_mnmajor(slot(u + h), ks), idO,
                    (e > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bar(L::bEmpty + u % L::kSlots));
-        mma_commit(bar(L::bEmpty + (u + 1) % L::kSlots));
+        release_units();
         mma_commit(bar(L::bPV + (e & 1)));
-        u += 2;
         return true;
       };
       if (len > 0 && ok) {
@@ -306,7 +320,7 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t tO = tmem + 256u + lane_off;
         uint32_t u[32];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           tmem_ld32(tO + 32u * cc, u);
           tmem_ld_wait(u);
 #pragma unroll
@@ -351,7 +365,7 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
     uint8_t* stage = smem + L::kQ;
 #pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
+    for (int cc = 0; cc < D / 32; ++cc) {
       uint32_t u[32];
       if (have_o) {
         tmem_ld32(tmem + 256u + lane_off + 32u * cc, u);
@@ -383,7 +397,7 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (lane == 0) {
       const int row0 = kTile * qi + 32 * warp;
       if (row0 < p.N)
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < D / 64; ++a)
           if (64 * a < p.d) tma_store_3d(&to, sbase + L::kQ + a * 16384 + 4096 * warp, 64 * a, row0, bh);
       bulk_commit_group();
       bulk_wait_group_read_all();
@@ -848,21 +862,31 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
 }  // namespace
 
-cudaError_t launch_fwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
+template <int D>
+cudaError_t launch_fwd_single_d(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static PerDeviceOnce smem_set[2];
-  auto kern = f16 ? fa_fwd_wide_kernel<true> : fa_fwd_wide_kernel<false>;
+  auto kern = f16 ? fa_fwd_wide_kernel<D, true> : fa_fwd_wide_kernel<D, false>;
   e = once_per_device(smem_set[f16 ? 1 : 0], dev, [&] {
-    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WFwdLayout::kSmemBytes);
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WFwdLayout<D>::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   FwdParams q = p;
   q.group = l2_head_group(4.0 * p.N * p.d, p.B * p.H);
   const dim3 grid((unsigned)(p.nT * p.B * p.H));
-  return launch_pdl(true, kern, grid, dim3(kWFwdThreads), WFwdLayout::kSmemBytes, s, tq, tk, tv, to, q);
+  return launch_pdl(true, kern, grid, dim3(kWFwdThreads), WFwdLayout<D>::kSmemBytes, s, tq, tk, tv, to, q);
+}
+
+// Only the 256-column instance is used: at 64 and 128 columns the two-Q-tile
+// kernel of fa_fwd.cu was measured faster (per-CTA set-up and epilogue are
+// paid twice as often with one Q tile per CTA).
+cudaError_t launch_fwd_single(int kd, bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& to, const FwdParams& p, cudaStream_t s) {
+  if (kd == 256) return launch_fwd_single_d<256>(f16, tq, tk, tv, to, p, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_wide(bool f16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
