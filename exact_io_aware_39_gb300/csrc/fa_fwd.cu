@@ -54,6 +54,12 @@ struct FwdLayout {
   // that read K come first
   static constexpr int kStagesK = (D == 64) ? 6 : 3;
   static constexpr int kStagesV = (D == 64) ? 5 : 2;
+  // At d = 64, S_0, S_1 (128 columns each) and O_0, O_1 (64 each) leave 128
+  // TMEM columns, which give each Q tile's P columns of their own: S_t is then
+  // free as soon as its softmax group has read it into registers, and the
+  // next S_t is computed while that group works on this one. At d = 128 the
+  // four regions fill TMEM and P is packed over S in place.
+  static constexpr bool kOwnP = (D == 64);
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
@@ -67,7 +73,9 @@ struct FwdLayout {
   static constexpr int bSFull = bVEmpty + kStagesV;   // [2]
   static constexpr int bPFull = bSFull + 2;           // [2]
   static constexpr int bOFinal = bPFull + 2;          // [2]
-  static constexpr int bDrain = bOFinal + 2;
+  static constexpr int bSFree = bOFinal + 2;          // [2] S_t read into registers (own P columns only)
+  static constexpr int bPVDone = bSFree + 2;          // [2] O_t += P_t V complete (own P columns only)
+  static constexpr int bDrain = bPVDone + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, list length, wait limit
   static constexpr int kList = kMisc + 16;           // uint16 entries
@@ -121,7 +129,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1) ? 4u : 1u);   // 4 = warps
+      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1 || i == L::bSFree || i == L::bSFree + 1) ? 4u
+                                                                                                      : 1u);   // 4 = warps
     abort_flag[0] = 0u;
     abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
@@ -222,50 +231,55 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     // tile's products. A pending PV is issued at the very next entry, so each
     // V slot is released one entry after its load and the K slot of entry e
     // right after its S products.
-    if (lane == 0) {
+    {   // the whole warp runs the schedule; one elected lane issues each MMA and commit
       constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
       constexpr uint32_t idO = idesc_16<F16>(128, D, false, true);
       const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
       const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+      // P_t: over S_t, or in columns of its own (after O_1)
+      const uint32_t tP[2] = {L::kOwnP ? tmem + 256u + 2u * D : tS[0], L::kOwnP ? tmem + 320u + 2u * D : tS[1]};
       const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
       const uint64_t dK0 = desc_kmajor(sbase + L::kK, 0);
       const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
       constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
       int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
       uint32_t npv[2] = {0u, 0u};   // PV groups issued per Q tile
-      bool ok = mbar_wait(bar(L::bQFull), 0, ctl, 4);
+      bool ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 4);
       tc_fence_after();
 
       // O_t += P_t V_{entry pe}
       auto issue_pv = [&](int t, int pe) -> bool {
         const int sv = pe % L::kStagesV;
-        if (!mbar_wait(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
-        if (!mbar_wait(bar(L::bVFull + sv), (uint32_t)(pe / L::kStagesV) & 1u, ctl, 6)) return false;
+        if (!mbar_wait_warp(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
+        if (!mbar_wait_warp(bar(L::bVFull + sv), (uint32_t)(pe / L::kStagesV) & 1u, ctl, 6)) return false;
         tc_fence_after();
         const uint64_t dV = dV0 + (uint64_t)sv * kSlotStep;
         const uint32_t acc0 = npv[t] > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts(tO[t], tS[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
+          mma_ts_w(tO[t], tP[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
+        if constexpr (L::kOwnP) mma_commit_w(bar(L::bPVDone + t));   // P_t may be rewritten, O_t rescaled
         ++npv[t];
         return true;
       };
 
-      for (int e = 0; e < len && ok; ++e) {
-        const uint32_t ent = list[e];
-        const int sk = e % L::kStagesK;
-        bool k_ready = false;
+      if constexpr (L::kOwnP) {
+        // Own P columns: at entry e, first S_t(e) for each live tile, each as
+        // soon as group t has read its previous S_t into registers, then the
+        // PVs of entry e - 1. For dense rows:
+        //   S0(e), S1(e), PV0(e-1), PV1(e-1), S0(e+1), ...
+        // so S_t(e+1) is computed while group t still works on S_t(e).
+        uint32_t ns[2] = {0u, 0u};   // S products issued per Q tile
+        for (int e = 0; e < len && ok; ++e) {
+          const uint32_t ent = list[e];
+          const int sk = e % L::kStagesK;
+          bool k_ready = false;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok) break;
-          if (prev[t] >= 0) {
-            ok = issue_pv(t, prev[t]);
-            prev[t] = -1;
-            if (!ok) break;
-          }
-          if (entry_live(ent, t)) {
+          for (int t = 0; t < 2; ++t) {
+            if (!ok || !entry_live(ent, t)) continue;
+            if (ns[t] > 0 && !(ok = mbar_wait_warp(bar(L::bSFree + t), (ns[t] - 1u) & 1u, ctl, 8))) break;
             if (!k_ready) {
-              ok = mbar_wait(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
+              ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
               if (!ok) break;
               tc_fence_after();
               k_ready = true;
@@ -273,24 +287,62 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const uint64_t dK = dK0 + (uint64_t)sk * kSlotStep;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              mma_ss(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
-            mma_commit(bar(L::bSFull + t));
-            prev[t] = e;
+              mma_ss_w(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
+            mma_commit_w(bar(L::bSFull + t));
+            ++ns[t];
           }
+          if (!ok) break;
+          mma_commit_w(bar(L::bKEmpty + sk));   // K_e is no longer needed
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
+            prev[t] = entry_live(ent, t) ? e : -1;
+          }
+          if (!ok) break;
+          if (e > 0) mma_commit_w(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
         }
-        if (!ok) break;
-        mma_commit(bar(L::bKEmpty + sk));                       // K_e is no longer needed
-        if (e > 0) mma_commit(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
+      } else {
+        for (int e = 0; e < len && ok; ++e) {
+          const uint32_t ent = list[e];
+          const int sk = e % L::kStagesK;
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) break;
+            if (prev[t] >= 0) {
+              ok = issue_pv(t, prev[t]);
+              prev[t] = -1;
+              if (!ok) break;
+            }
+            if (entry_live(ent, t)) {
+              if (!k_ready) {
+                ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              const uint64_t dK = dK0 + (uint64_t)sk * kSlotStep;
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_ss_w(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
+              mma_commit_w(bar(L::bSFull + t));
+              prev[t] = e;
+            }
+          }
+          if (!ok) break;
+          mma_commit_w(bar(L::bKEmpty + sk));                       // K_e is no longer needed
+          if (e > 0) mma_commit_w(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
+        }
       }
       if (ok) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
-          if (ok && npv[t] > 0) mma_commit(bar(L::bOFinal + t));
+          if (ok && npv[t] > 0) mma_commit_w(bar(L::bOFinal + t));
         }
       }
-      // every MMA this thread issued must be complete before TMEM is freed
-      mma_commit(bar(L::bDrain));
+      // every MMA this warp issued must be complete before TMEM is freed
+      mma_commit_w(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
   } else if (warp < 8) {
@@ -303,6 +355,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_off;
     const uint32_t tO = tmem + 256u + (uint32_t)(t * D) + lane_off;
+    const uint32_t tP = L::kOwnP ? tmem + 256u + 2u * D + 64u * (uint32_t)t + lane_off : tS;
     const float sl2 = p.scale_log2;
 
     float m_ref = -INFINITY;
@@ -337,6 +390,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           x[96 + i] = __uint_as_float(u3[i]);
         }
       }
+      if constexpr (L::kOwnP) {   // S_t is in registers: the next S_t may be computed
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::bSFree + t));
+      }
       if (entry_partial(ent, t)) {
         const int key0 = kTile * entry_j(ent);
 #pragma unroll
@@ -366,6 +423,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
         l *= alpha;
         m_ref = m_new;
+      }
+      if (L::kOwnP && n > 0) {
+        // the previous O_t += P_t V has completed: O_t may be rescaled and
+        // the P_t columns rewritten
+        if (!mbar_wait_warp(bar(L::bPVDone + t), (n - 1u) & 1u, ctl, 16 + t)) { ok = false; break; }
+        tc_fence_after();
       }
       if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
         uint32_t u[32];
@@ -421,7 +484,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             pk[i] = pack2<F16>(p0, p1);
           }
         }
-        tmem_st32(tS + 32u * hh, pk);
+        tmem_st32(tP + 32u * hh, pk);
       }
       tmem_st_wait();
       const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);

@@ -192,25 +192,25 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {   // the whole warp runs the schedule; one elected lane issues each MMA and commit
       constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
       constexpr uint32_t idO = idesc_16<F16>(128, L::kU, false, true);
       constexpr int kStepsPerUnit = L::kU / 16;
       const uint32_t tS[2] = {tmem, tmem + 128u};
       const uint32_t tO = tmem + 256u;
       const uint64_t dQ0 = desc_kmajor(sbase + L::kQ, 0);
-      bool ok = mbar_wait(bar(L::bQFull), 0, ctl, 44);
+      bool ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 44);
       tc_fence_after();
       int u = 0;
       auto slot = [&](int uu) -> uint32_t { return sbase + L::kRing + (uint32_t)(uu % L::kSlots) * L::kUnitBytes; };
       auto wait_units = [&](uint32_t site) -> bool {
         for (int unit = 0; unit < L::kUnits; ++unit)
-          if (!mbar_wait(bar(L::bFull + (u + unit) % L::kSlots), (uint32_t)((u + unit) / L::kSlots) & 1u, ctl, site))
+          if (!mbar_wait_warp(bar(L::bFull + (u + unit) % L::kSlots), (uint32_t)((u + unit) / L::kSlots) & 1u, ctl, site))
             return false;
         return true;
       };
       auto release_units = [&]() {
-        for (int unit = 0; unit < L::kUnits; ++unit) mma_commit(bar(L::bEmpty + (u + unit) % L::kSlots));
+        for (int unit = 0; unit < L::kUnits; ++unit) mma_commit_w(bar(L::bEmpty + (u + unit) % L::kSlots));
         u += L::kUnits;
       };
       // S(e) = Q K_e^T into buffer e mod 2 (K in units u ..)
@@ -219,25 +219,25 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tS[e & 1], dQ0 + kmajor_step(ks), desc_kmajor(slot(u + ks / kStepsPerUnit), ks % kStepsPerUnit), idS,
+          mma_ss_w(tS[e & 1], dQ0 + kmajor_step(ks), desc_kmajor(slot(u + ks / kStepsPerUnit), ks % kStepsPerUnit), idS,
                  ks > 0 ? 1u : 0u);
         release_units();
-        mma_commit(bar(L::bSFull + (e & 1)));
+        mma_commit_w(bar(L::bSFull + (e & 1)));
         return true;
       };
       // O += P(e) V_e (V in units u ..: output columns kU h .. kU h + kU - 1)
       auto issue_pv = [&](int e) -> bool {
-        if (!mbar_wait(bar(L::bPFull + (e & 1)), (uint32_t)(e >> 1) & 1u, ctl, 46)) return false;
+        if (!mbar_wait_warp(bar(L::bPFull + (e & 1)), (uint32_t)(e >> 1) & 1u, ctl, 46)) return false;
         if (!wait_units(47)) return false;
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < L::kUnits; ++h)
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ts(tO + (uint32_t)(L::kU * h), tS[e & 1] + (uint32_t)ks * 8u, desc_mnmajor(slot(u + h), ks), idO,
+            mma_ts_w(tO + (uint32_t)(L::kU * h), tS[e & 1] + (uint32_t)ks * 8u, desc_mnmajor(slot(u + h), ks), idO,
                    (e > 0 || ks > 0) ? 1u : 0u);
         release_units();
-        mma_commit(bar(L::bPV + (e & 1)));
+        mma_commit_w(bar(L::bPV + (e & 1)));
         return true;
       };
       if (len > 0 && ok) {
@@ -246,9 +246,9 @@ fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (e + 1 < len && !(ok = issue_s(e + 1))) break;
           ok = issue_pv(e);
         }
-        if (ok) mma_commit(bar(L::bOFinal));
+        if (ok) mma_commit_w(bar(L::bOFinal));
       }
-      mma_commit(bar(L::bDrain));
+      mma_commit_w(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
   } else {
