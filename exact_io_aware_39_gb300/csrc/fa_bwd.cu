@@ -315,15 +315,18 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const uint32_t sdS = sbase + L::kdS;
       bool ok = true;
       int g = 0;
+      // Shared-memory descriptors are built as a base plus a constant step per
+      // K step wherever that keeps within the MMA thread's registers, so that
+      // issuing an MMA costs the thread one 64-bit add.
       // S^T = K Q^T of running query tile g
       auto issue_s = [&](uint32_t sK, int g1) -> bool {
         const int s1 = g1 % L::kStages;
         if (!mbar_wait(bar(L::bQFull + s1), (uint32_t)(g1 / L::kStages) & 1u, ctl, 114)) return false;
         tc_fence_after();
-        const uint32_t sQ1 = sbase + L::kQ + s1 * L::kTileBytes;
+        const uint64_t dK0 = desc_kmajor(sK, 0), dQ0 = desc_kmajor(sbase + L::kQ + s1 * L::kTileBytes, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tS, desc_kmajor(sK, ks), desc_kmajor(sQ1, ks), idSP, ks > 0 ? 1u : 0u);
+          mma_ss(tS, dK0 + kmajor_step(ks), dQ0 + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
         mma_commit(bar(L::bSFull));
         return true;
       };
@@ -334,6 +337,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (i >= p.nT) continue;
         const int kb = k % L::kKV;
         const uint32_t sK = sbase + L::kK + kb * L::kKVBytes, sV = sbase + L::kV + kb * L::kKVBytes;
+        const uint64_t mK = desc_mnmajor(sK, 0);
         if (!(ok = mbar_wait(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 110))) break;
         if (!(ok = issue_s(sK, g))) break;
         for (int it = 0; i < p.nT; ++it, ++g) {
@@ -346,18 +350,20 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (!kOwnDQ && g > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
           if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 116))) break;
           tc_fence_after();
+          const uint64_t kdV = desc_kmajor(sV, 0), kdO = desc_kmajor(sdO, 0);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tP, desc_kmajor(sV, ks), desc_kmajor(sdO, ks), idSP, ks > 0 ? 1u : 0u);
+            mma_ss(tP, kdV + kmajor_step(ks), kdO + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
           mma_commit(bar(L::bdPFull));
           // dV += P^T dO (at it == 0 over the previous item's dV and dK, which
           // the compute warps have read out of TMEM before arriving on this P)
           if (!(ok = mbar_wait(bar(L::bPFull), (uint32_t)g & 1u, ctl, 113))) break;
           tc_fence_after();
+          const uint64_t mdO = desc_mnmajor(sdO, 0);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
-            mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sdO, ks), idV,
+            mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mdO + mnmajor_step(ks), idV,
                    (it > 0 || ks > 0) ? 1u : 0u);
           // next S^T of this item: at d = 64 right behind dV (the tensor pipe
           // runs in issue order, so dV has read P first), so that P of the
@@ -367,10 +373,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // dK += dS^T Q ; dQ_i = dS K
           if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)g & 1u, ctl, 115))) break;
           tc_fence_after();
+          const uint64_t mQ = desc_mnmajor(sQ, 0);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             // dS^T of queries 0-63 in columns tDS + 0..31, of queries 64-127 in tDS + 64..95
-            mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), desc_mnmajor(sQ, ks), idK,
+            mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mQ + mnmajor_step(ks), idK,
                    (it > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
           // at d = 64 the previous dQ partial must have been read out of its columns
@@ -378,7 +385,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ss(tQ, desc_mnmajor(sdS, ks), desc_mnmajor(sK, ks), idQ, ks > 0 ? 1u : 0u);
+            mma_ss(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
           mma_commit(bar(L::bdQFull));
           mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
           if (!kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
