@@ -307,7 +307,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // At d = 128 the whole warp runs the schedule and one elected lane issues
+    // each MMA and commit; at d = 64 one lane runs it (measured: the warp-wide
+    // form is 1.5 % faster at d = 128 and 2-3 % slower at d = 64).
+    constexpr bool kW = (D == 128);
+    if (kW || lane == 0) {
       constexpr uint32_t idSP = idesc_16<F16>(128, 128, false, false);
       constexpr uint32_t idV = idesc_16<F16>(128, D, false, true);
       constexpr uint32_t idK = idesc_16<F16>(128, D, false, true);
@@ -321,24 +325,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       // S^T = K Q^T of running query tile g
       auto issue_s = [&](uint32_t sK, int g1) -> bool {
         const int s1 = g1 % L::kStages;
-        if (!mbar_wait(bar(L::bQFull + s1), (uint32_t)(g1 / L::kStages) & 1u, ctl, 114)) return false;
+        if (!mbar_wait_t<kW>(bar(L::bQFull + s1), (uint32_t)(g1 / L::kStages) & 1u, ctl, 114)) return false;
         tc_fence_after();
         const uint64_t dK0 = desc_kmajor(sK, 0), dQ0 = desc_kmajor(sbase + L::kQ + s1 * L::kTileBytes, 0);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tS, dK0 + kmajor_step(ks), dQ0 + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
-        mma_commit(bar(L::bSFull));
+          mma_ss_t<kW>(tS, dK0 + kmajor_step(ks), dQ0 + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
+        mma_commit_t<kW>(bar(L::bSFull));
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const Item w = take_item(k, false, ok);
+        const Item w = take_item(k, kW, ok);
         if (w.kj < 0) break;
         int i = next_live(w, 0);
         if (i >= p.nT) continue;
         const int kb = k % L::kKV;
         const uint32_t sK = sbase + L::kK + kb * L::kKVBytes, sV = sbase + L::kV + kb * L::kKVBytes;
         const uint64_t mK = desc_mnmajor(sK, 0);
-        if (!(ok = mbar_wait(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 110))) break;
+        if (!(ok = mbar_wait_t<kW>(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 110))) break;
         if (!(ok = issue_s(sK, g))) break;
         for (int it = 0; i < p.nT; ++it, ++g) {
           const int inext = next_live(w, i + 1);
@@ -347,23 +351,23 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const uint32_t sdO = sbase + L::kdO + s * L::kTileBytes;
           // dP^T = V dO^T (at d = 128 the dQ partial of the previous tile must
           // have been read out of these columns)
-          if (!kOwnDQ && g > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
-          if (!(ok = mbar_wait(bar(L::bdOFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 116))) break;
+          if (!kOwnDQ && g > 0 && !(ok = mbar_wait_t<kW>(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
+          if (!(ok = mbar_wait_t<kW>(bar(L::bdOFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 116))) break;
           tc_fence_after();
           const uint64_t kdV = desc_kmajor(sV, 0), kdO = desc_kmajor(sdO, 0);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tP, kdV + kmajor_step(ks), kdO + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
-          mma_commit(bar(L::bdPFull));
+            mma_ss_t<kW>(tP, kdV + kmajor_step(ks), kdO + kmajor_step(ks), idSP, ks > 0 ? 1u : 0u);
+          mma_commit_t<kW>(bar(L::bdPFull));
           // dV += P^T dO (at it == 0 over the previous item's dV and dK, which
           // the compute warps have read out of TMEM before arriving on this P)
-          if (!(ok = mbar_wait(bar(L::bPFull), (uint32_t)g & 1u, ctl, 113))) break;
+          if (!(ok = mbar_wait_t<kW>(bar(L::bPFull), (uint32_t)g & 1u, ctl, 113))) break;
           tc_fence_after();
           const uint64_t mdO = desc_mnmajor(sdO, 0);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
-            mma_ts(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mdO + mnmajor_step(ks), idV,
+            mma_ts_t<kW>(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mdO + mnmajor_step(ks), idV,
                    (it > 0 || ks > 0) ? 1u : 0u);
           // next S^T of this item: at d = 64 right behind dV (the tensor pipe
           // runs in issue order, so dV has read P first), so that P of the
@@ -371,29 +375,29 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // d = 128 after dQ, which leaves the next Q load the longest window
           if (kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
           // dK += dS^T Q ; dQ_i = dS K
-          if (!(ok = mbar_wait(bar(L::bdSFull), (uint32_t)g & 1u, ctl, 115))) break;
+          if (!(ok = mbar_wait_t<kW>(bar(L::bdSFull), (uint32_t)g & 1u, ctl, 115))) break;
           tc_fence_after();
           const uint64_t mQ = desc_mnmajor(sQ, 0);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             // dS^T of queries 0-63 in columns tDS + 0..31, of queries 64-127 in tDS + 64..95
-            mma_ts(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mQ + mnmajor_step(ks), idK,
+            mma_ts_t<kW>(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mQ + mnmajor_step(ks), idK,
                    (it > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
+          mma_commit_t<kW>(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
           // at d = 64 the previous dQ partial must have been read out of its columns
-          if (kOwnDQ && g > 0 && !(ok = mbar_wait(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
+          if (kOwnDQ && g > 0 && !(ok = mbar_wait_t<kW>(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ss(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
-          mma_commit(bar(L::bdQFull));
-          mma_commit(bar(L::bdSEmpty));      // dK and dQ have read dS
+            mma_ss_t<kW>(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
+          mma_commit_t<kW>(bar(L::bdQFull));
+          mma_commit_t<kW>(bar(L::bdSEmpty));      // dK and dQ have read dS
           if (!kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
           i = inext;
         }
-        if (ok) mma_commit(bar(L::bFinal));   // dV and dK of the item are complete
+        if (ok) mma_commit_t<kW>(bar(L::bFinal));   // dV and dK of the item are complete
       }
-      mma_commit(bar(L::bDrain));
+      mma_commit_t<kW>(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
   } else if (warp < 8) {

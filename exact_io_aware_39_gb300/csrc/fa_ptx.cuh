@@ -158,6 +158,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+template <bool W>
+__device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t site) {
+  if constexpr (W) return mbar_wait_warp(bar, parity, c, site);
+  else return mbar_wait(bar, parity, c, site);
+}
+
 // Bounded wait that ignores the abort flag: used on exit paths to let copies
 // and MMAs that were already issued finish before shared memory or TMEM is
 // released.
@@ -313,6 +319,26 @@ __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
       :: "r"(bar) : "memory");
+}
+
+// The same calls with the issuing form chosen at compile time: the whole
+// warp (W = true, the _w forms and warp-collective waits) or one lane.
+template <bool W>
+__device__ __forceinline__ void mma_ss_t(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  if constexpr (W) mma_ss_w(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else mma_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+template <bool W>
+__device__ __forceinline__ void mma_ts_t(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  if constexpr (W) mma_ts_w(d_tmem, a_tmem, b_desc, idesc, accumulate);
+  else mma_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+}
+template <bool W>
+__device__ __forceinline__ void mma_commit_t(uint32_t bar) {
+  if constexpr (W) mma_commit_w(bar);
+  else mma_commit(bar);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32
