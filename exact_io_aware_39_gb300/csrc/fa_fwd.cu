@@ -77,8 +77,9 @@ struct FwdLayout {
   static constexpr int bPVDone = bSFree + 2;          // [2] O_t += P_t V complete (own P columns only)
   static constexpr int bDrain = bPVDone + 2;
   static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, list length, wait limit
-  static constexpr int kList = kMisc + 16;           // uint16 entries
+  // tmem slot, abort flag, list length, wait limit, last list entry live for Q tile 0 and 1
+  static constexpr int kMisc = kBar + 8 * kNumBars;
+  static constexpr int kList = kMisc + 32;           // uint16 entries
   static constexpr int kSmemBytes = kList + 2 * kListMax;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -139,14 +140,29 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
+  __syncthreads();   // the barriers are initialised: the producer may start loading
   // global memory is read and written only from here on: what the previous
   // kernel in the stream wrote is complete and visible
   grid_dep_wait();
   grid_dep_launch();
   const int kvl = effective_kv_len(p.kv_len, b, p.N);
+  int nk = 0;   // K loads issued (producer thread)
   if (warp == 8) {
-    // union list of live key tiles of the two Q tiles, ascending j
+    // Q first, then the union list of live key tiles of the two Q tiles
+    // (ascending j), then the K tiles of the first ring's worth of entries:
+    // their loads overlap the rest of the set-up
+    if (lane == 0) {
+      tma_prefetch_map(&tq);
+      tma_prefetch_map(&tk);
+      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
+      mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
+      for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
+                      kTile * (qi0 + t), bh);
+    }
     int count = 0;
+    int last[2] = {-1, -1};
     for (int base = 0; base < p.nT; base += 32) {
       const int j = base + lane;
       uint32_t e = 0;
@@ -159,9 +175,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       const bool live = (e >> 10) & 3u;
       const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
       if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {   // list index of the last entry live for Q tile t so far
+        const uint32_t bt = __ballot_sync(0xFFFFFFFFu, (e >> (10 + t)) & 1u);
+        if (bt != 0u) last[t] = count + __popc(ball & ((1u << (31 - __clz(bt))) - 1u));
+      }
       count += __popc(ball);
     }
-    if (lane == 0) misc[2] = (uint32_t)count;
+    __syncwarp();
+    if (lane == 0) {
+      misc[2] = (uint32_t)count;
+      misc[4] = (uint32_t)last[0];
+      misc[5] = (uint32_t)last[1];
+      for (; nk < count && nk < L::kStagesK; ++nk) {   // the first use of each ring slot: no wait
+        if (p.chk.stall != 0u && nk >= 1) break;      // test of the timeout path: K of entry 1 never comes
+        mbar_arrive_expect_tx(bar(L::bKFull + nk), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(sbase + L::kK + nk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + nk), 64 * h,
+                      kTile * entry_j(list[nk]), bh);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -174,16 +207,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   if (warp == 8) {
     // ------------------------------------------------------------ Q and K producer
     if (lane == 0) {
-      tma_prefetch_map(&tq);
-      tma_prefetch_map(&tk);
-      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
-      mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
-      for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
-                      kTile * (qi0 + t), bh);
-      int nk = 0;   // K loads issued
-      for (int e = 0; e < len; ++e) {
+      // Q and the first entries' K were issued during the set-up
+      for (int e = nk; e < len; ++e) {
         if (p.chk.stall != 0u && e >= 1) break;   // test of the timeout path: K of entry 1 never comes
         const int j = entry_j(list[e]);
         const int sk = e % L::kStagesK;
@@ -243,6 +268,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
       constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
       int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
+      // the last entry live for each Q tile: its PV completes O_t, which the
+      // softmax group may then read out while the other tile's products run
+      const int lastE[2] = {(int)misc[4], (int)misc[5]};
       uint32_t npv[2] = {0u, 0u};   // PV groups issued per Q tile
       bool ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 4);
       tc_fence_after();
@@ -259,6 +287,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int ks = 0; ks < kTile / 16; ++ks)
           mma_ts_w(tO[t], tP[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
         if constexpr (L::kOwnP) mma_commit_w(bar(L::bPVDone + t));   // P_t may be rewritten, O_t rescaled
+        if (pe == lastE[t]) mma_commit_w(bar(L::bOFinal + t));       // O_t is complete
         ++npv[t];
         return true;
       };
@@ -337,8 +366,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       if (ok) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
-          if (ok && npv[t] > 0) mma_commit_w(bar(L::bOFinal + t));
+          if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);   // (commits O_t's completion)
         }
       }
       // every MMA this warp issued must be complete before TMEM is freed
