@@ -20,7 +20,7 @@ enum TileState : int { kSkip = 0, kFull = 1, kPartial = 2 };
 
 // Device error word layout: [0] = first error code (0 = none), [1] = site id,
 // [2] = blockIdx.x of the reporting CTA, [3] = threadIdx.x.
-enum DeviceErr : uint32_t { kErrNone = 0, kErrTimeout = 5, kErrSmemAlign = 6 };
+enum DeviceErr : uint32_t { kErrNone = 0, kErrTimeout = 5, kErrSmemAlign = 6, kErrInternal = 6 };
 
 // State of the (query tile qi, key tile kj) pair. kvl is the effective key
 // length of the batch entry, already clamped to [0, N]; bm is the block mask

@@ -75,11 +75,14 @@ struct FwdLayout {
   static constexpr int bOFinal = bPFull + 2;          // [2]
   static constexpr int bSFree = bOFinal + 2;          // [2] S_t read into registers (own P columns only)
   static constexpr int bPVDone = bSFree + 2;          // [2] O_t += P_t V complete (own P columns only)
-  static constexpr int bDrain = bPVDone + 2;
+  static constexpr int bClc = bPVDone + 2;            // the next item's cancellation answer has arrived
+  static constexpr int bDrain = bClc + 1;
   static constexpr int kNumBars = bDrain + 1;
-  // tmem slot, abort flag, list length, wait limit, last list entry live for Q tile 0 and 1
+  // tmem slot, abort flag, list length, wait limit, last list entry live for
+  // Q tile 0 and 1, next item, -
   static constexpr int kMisc = kBar + 8 * kNumBars;
-  static constexpr int kList = kMisc + 32;           // uint16 entries
+  static constexpr int kClc = (kMisc + 32 + 15) & ~15;   // 16-byte answer of a launch cancellation
+  static constexpr int kList = kClc + 16;                // uint16 entries
   static constexpr int kSmemBytes = kList + 2 * kListMax;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -105,13 +108,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   const int BH = p.B * p.H;
   const int nC = (p.nT + 1) >> 1;
-  // CTAs walk groups of p.group heads whose K and V fit in L2 together;
-  // within a group the heaviest Q-tile pairs come first
-  int bh = 0;
-  const int c = nC - 1 - split_grouped((int)blockIdx.x, p.group, nC, BH, &bh);
-  const int b = bh / p.H;
-  const int qi0 = 2 * c;
-  const bool has_t1 = (qi0 + 1) < p.nT;
 
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -140,212 +136,261 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
-  __syncthreads();   // the barriers are initialised: the producer may start loading
+  tc_fence_before();
+  __syncthreads();   // the barriers are initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
   // global memory is read and written only from here on: what the previous
   // kernel in the stream wrote is complete and visible
   grid_dep_wait();
   grid_dep_launch();
-  const int kvl = effective_kv_len(p.kv_len, b, p.N);
-  int nk = 0;   // K loads issued (producer thread)
+
+  // Persistent over items (pairs of Q tiles of one batch-head): the first is
+  // this CTA's own, each further one is a CTA of this grid that has not
+  // started yet, cancelled through cluster launch control (so items are
+  // taken in launch order, each by the first CTA ready for one, and no
+  // workspace counter is needed). The CTAs walk groups of p.group heads
+  // whose K and V fit in L2 together; within a group the heaviest Q-tile
+  // pairs come first. Every ring and barrier phase runs on across items:
+  // eK / eV count the K / V ring entries of the items before this one, and
+  // each role keeps its own running counts.
+  int eK = 0, eV = 0;
+  int nk = 0, nv = 0;                     // K / V loads issued (producer threads)
+  bool clc_out = false;                   // a cancellation answer is outstanding (K producer)
+  uint32_t ns[2] = {0u, 0u}, npv[2] = {0u, 0u};   // S and PV groups issued per Q tile (MMA warp)
+  uint32_t nS = 0u, nOF = 0u;             // S tiles and final O read by this softmax group
+  int item = (int)blockIdx.x;
+  uint32_t kq = 0u;                       // items started: the phase of the Q barrier
+  // The roles meet at a named barrier before each item (its list is in
+  // shared memory) and after it (its O is stored, its products read out).
+  auto item_sync = [&]() {
+    tc_fence_before();
+    named_bar_sync(1, kFwdThreads);
+    tc_fence_after();
+  };
+  // after an item: the next one, or none (then every role leaves its loop)
+  auto next_item = [&]() -> int {
+    const int next = (int)misc[6];
+    return abort_flag[0] != 0u ? -1 : next;
+  };
   if (warp == 8) {
-    // Q first, then the union list of live key tiles of the two Q tiles
-    // (ascending j), then the K tiles of the first ring's worth of entries:
-    // their loads overlap the rest of the set-up
-    if (lane == 0) {
-      tma_prefetch_map(&tq);
-      tma_prefetch_map(&tk);
-      const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
-      mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
-      for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
-                      kTile * (qi0 + t), bh);
-    }
-    int count = 0;
-    int last[2] = {-1, -1};
-    for (int base = 0; base < p.nT; base += 32) {
-      const int j = base + lane;
-      uint32_t e = 0;
-      if (j < p.nT) {
-        const int s0 = tile_state(qi0, j, kvl, p.nT, p.causal, p.block_mask);
-        const int s1 = has_t1 ? tile_state(qi0 + 1, j, kvl, p.nT, p.causal, p.block_mask) : kSkip;
-        e = (uint32_t)j | ((s0 != kSkip) ? (1u << 10) : 0u) | ((s1 != kSkip) ? (1u << 11) : 0u) |
-            ((s0 == kPartial) ? (1u << 12) : 0u) | ((s1 == kPartial) ? (1u << 13) : 0u);
+    regs_dec<kOtherRegs>();
+    for (;; ++kq) {
+      int bh = 0;
+      const int c = nC - 1 - split_grouped(item, p.group, nC, BH, &bh);
+      const int b = bh / p.H;
+      const int qi0 = 2 * c;
+      const bool has_t1 = (qi0 + 1) < p.nT;
+      const int kvl = effective_kv_len(p.kv_len, b, p.N);
+      int kpre = 0;   // K loads of this item issued during its set-up (producer thread)
+      // Q first, then the union list of live key tiles of the two Q tiles
+      // (ascending j), then the K tiles of the first ring's worth of entries:
+      // their loads overlap the rest of the set-up
+      if (lane == 0) {
+        if (kq == 0u) {
+          tma_prefetch_map(&tq);
+          tma_prefetch_map(&tk);
+        }
+        const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
+        mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
+        for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
+                        kTile * (qi0 + t), bh);
       }
-      const bool live = (e >> 10) & 3u;
-      const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
-      if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+      int count = 0;
+      int last[2] = {-1, -1};
+      for (int base = 0; base < p.nT; base += 32) {
+        const int j = base + lane;
+        uint32_t e = 0;
+        if (j < p.nT) {
+          const int s0 = tile_state(qi0, j, kvl, p.nT, p.causal, p.block_mask);
+          const int s1 = has_t1 ? tile_state(qi0 + 1, j, kvl, p.nT, p.causal, p.block_mask) : kSkip;
+          e = (uint32_t)j | ((s0 != kSkip) ? (1u << 10) : 0u) | ((s1 != kSkip) ? (1u << 11) : 0u) |
+              ((s0 == kPartial) ? (1u << 12) : 0u) | ((s1 == kPartial) ? (1u << 13) : 0u);
+        }
+        const bool live = (e >> 10) & 3u;
+        const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
+        if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {   // list index of the last entry live for Q tile t so far
-        const uint32_t bt = __ballot_sync(0xFFFFFFFFu, (e >> (10 + t)) & 1u);
-        if (bt != 0u) last[t] = count + __popc(ball & ((1u << (31 - __clz(bt))) - 1u));
+        for (int t = 0; t < 2; ++t) {   // list index of the last entry live for Q tile t so far
+          const uint32_t bt = __ballot_sync(0xFFFFFFFFu, (e >> (10 + t)) & 1u);
+          if (bt != 0u) last[t] = count + __popc(ball & ((1u << (31 - __clz(bt))) - 1u));
+        }
+        count += __popc(ball);
       }
-      count += __popc(ball);
+      __syncwarp();
+      if (lane == 0) {
+        misc[2] = (uint32_t)count;
+        misc[4] = (uint32_t)last[0];
+        misc[5] = (uint32_t)last[1];
+        // K of the first ring's worth of entries: their loads overlap the rest
+        // of the set-up (the slots' previous users are complete: the previous
+        // item ended with all its products read out)
+        for (; kpre < count && kpre < L::kStagesK; ++kpre) {
+          if (p.chk.stall != 0u && kpre >= 1) break;   // test of the timeout path: K of entry 1 never comes
+          const int n = eK + kpre;
+          const int sk = n % L::kStagesK;
+          if (n >= L::kStagesK && !mbar_wait(bar(L::bKEmpty + sk), (uint32_t)(n / L::kStagesK - 1) & 1u, ctl, 1))
+            break;
+          mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk), 64 * h,
+                        kTile * entry_j(list[kpre]), bh);
+          ++nk;
+        }
+      }
+      item_sync();
+      const int len = (int)misc[2];
+      // ------------------------------------------------------------ Q and K producer
+      if (lane == 0) {
+        // K of ring entry eK + e into slot (eK + e) mod S, once the MMAs of the
+        // entry that used the slot before (of this item or an earlier one)
+        // have read it
+        bool ok = true;
+        for (int e = kpre; e < len; ++e) {
+          if (p.chk.stall != 0u && e >= 1) { ok = false; break; }   // test of the timeout path: K of entry 1 never comes
+          const int n = eK + e;
+          const int sk = n % L::kStagesK;
+          if (n >= L::kStagesK && !(ok = mbar_wait(bar(L::bKEmpty + sk), (uint32_t)(n / L::kStagesK - 1) & 1u, ctl, 1)))
+            break;
+          mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk),
+                        64 * h, kTile * entry_j(list[e]), bh);
+          ++nk;
+        }
+        // every K load of the item is issued: ask for the next item (the answer
+        // lands while this one is computed)
+        int next = -1;
+        if (ok) {
+          mbar_arrive_expect_tx(bar(L::bClc), 16u);
+          clc_try_cancel(sbase + L::kClc, bar(L::bClc));
+          clc_out = true;
+          if (mbar_wait(bar(L::bClc), kq & 1u, ctl, 3)) {
+            clc_out = false;
+            next = clc_first_ctaid_x(sbase + L::kClc);
+            if (next >= (int)gridDim.x) {   // not a CTA of this grid: stop rather than decode it
+              report_error(ctl, kErrInternal, 9);
+              next = -1;
+            }
+          }
+        }
+        misc[6] = (uint32_t)next;
+      }
+      item_sync();
+      item = next_item();
+      if (item < 0) break;
+      eK += len;
     }
-    __syncwarp();
+    // every load and cancellation request issued has completed before the
+    // CTA exits; loads were issued in ring order, so the last load into slot
+    // s was number s + S * floor((n - 1 - s) / S)
     if (lane == 0) {
-      misc[2] = (uint32_t)count;
-      misc[4] = (uint32_t)last[0];
-      misc[5] = (uint32_t)last[1];
-      for (; nk < count && nk < L::kStagesK; ++nk) {   // the first use of each ring slot: no wait
-        if (p.chk.stall != 0u && nk >= 1) break;      // test of the timeout path: K of entry 1 never comes
-        mbar_arrive_expect_tx(bar(L::bKFull + nk), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kK + nk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + nk), 64 * h,
-                      kTile * entry_j(list[nk]), bh);
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  const uint32_t tmem = misc[0];
-  const int len = (int)misc[2];
-
-  if (warp >= 8) regs_dec<kOtherRegs>();
-  if (warp == 8) {
-    // ------------------------------------------------------------ Q and K producer
-    if (lane == 0) {
-      // Q and the first entries' K were issued during the set-up
-      for (int e = nk; e < len; ++e) {
-        if (p.chk.stall != 0u && e >= 1) break;   // test of the timeout path: K of entry 1 never comes
-        const int j = entry_j(list[e]);
-        const int sk = e % L::kStagesK;
-        const uint32_t nk_ = (uint32_t)(e / L::kStagesK);
-        if (e >= L::kStagesK && !mbar_wait(bar(L::bKEmpty + sk), (nk_ - 1) & 1u, ctl, 1)) break;
-        mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk),
-                      64 * h, kTile * j, bh);
-        ++nk;
-      }
-      // every load issued must have landed before the CTA may exit; the last
-      // load into stage s was entry s + S * floor((n - 1 - s) / S)
-      drain_wait(bar(L::bQFull), 0);
+      drain_wait(bar(L::bQFull), kq & 1u);
       for (int s = 0; s < L::kStagesK && s < nk; ++s)
         drain_wait(bar(L::bKFull + s), (uint32_t)((nk - 1 - s) / L::kStagesK) & 1u);
+      if (clc_out) drain_wait(bar(L::bClc), kq & 1u);
     }
   } else if (warp == 10) {
-    // ------------------------------------------------------------ V producer
-    // (its own thread, so that the K ring can run ahead of the V ring)
-    if (lane == 0) {
-      tma_prefetch_map(&tv);
-      int nv = 0;   // V loads issued
-      for (int e = 0; e < len; ++e) {
-        const int j = entry_j(list[e]);
-        const int sv = e % L::kStagesV;
-        const uint32_t nv_ = (uint32_t)(e / L::kStagesV);
-        if (e >= L::kStagesV && !mbar_wait(bar(L::bVEmpty + sv), (nv_ - 1) & 1u, ctl, 2)) break;
-        mbar_arrive_expect_tx(bar(L::bVFull + sv), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_3d(sbase + L::kV + sv * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + sv),
-                      64 * h, kTile * j, bh);
-        ++nv;
+    regs_dec<kOtherRegs>();
+    for (;; ++kq) {
+      int bh = 0;
+      (void)split_grouped(item, p.group, nC, BH, &bh);
+      item_sync();
+      const int len = (int)misc[2];
+      // ------------------------------------------------------------ V producer
+      // (its own thread, so that the K ring can run ahead of the V ring)
+      if (lane == 0) {
+        if (kq == 0u) tma_prefetch_map(&tv);
+        for (int e = 0; e < len; ++e) {
+          const int n = eV + e;
+          const int sv = n % L::kStagesV;
+          if (n >= L::kStagesV && !mbar_wait(bar(L::bVEmpty + sv), (uint32_t)(n / L::kStagesV - 1) & 1u, ctl, 2))
+            break;
+          mbar_arrive_expect_tx(bar(L::bVFull + sv), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_3d(sbase + L::kV + sv * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + sv),
+                        64 * h, kTile * entry_j(list[e]), bh);
+          ++nv;
+        }
       }
+      item_sync();
+      item = next_item();
+      if (item < 0) break;
+      eV += len;
+    }
+    if (lane == 0)
       for (int s = 0; s < L::kStagesV && s < nv; ++s)
         drain_wait(bar(L::bVFull + s), (uint32_t)((nv - 1 - s) / L::kStagesV) & 1u);
-    }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // Fixed schedule over the union list: at entry e, for each Q tile t, first
-    // the pending O_t += P_t V of t's previous live entry (waiting for P_t),
-    // then S_t = Q_t K_e^T if t is live at e. For dense rows this is
-    //   PV0(e-1), S0(e), PV1(e-1), S1(e), PV0(e), ...
-    // so that while one softmax group works the tensor core runs the other
-    // tile's products. A pending PV is issued at the very next entry, so each
-    // V slot is released one entry after its load and the K slot of entry e
-    // right after its S products.
-    {   // the whole warp runs the schedule; one elected lane issues each MMA and commit
-      constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
-      constexpr uint32_t idO = idesc_16<F16>(128, D, false, true);
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
-      // P_t: over S_t, or in columns of its own (after O_1)
-      const uint32_t tP[2] = {L::kOwnP ? tmem + 256u + 2u * D : tS[0], L::kOwnP ? tmem + 320u + 2u * D : tS[1]};
-      const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
-      const uint64_t dK0 = desc_kmajor(sbase + L::kK, 0);
-      const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
-      constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
-      int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
-      // the last entry live for each Q tile: its PV completes O_t, which the
-      // softmax group may then read out while the other tile's products run
-      const int lastE[2] = {(int)misc[4], (int)misc[5]};
-      uint32_t npv[2] = {0u, 0u};   // PV groups issued per Q tile
-      bool ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 4);
-      tc_fence_after();
-
-      // O_t += P_t V_{entry pe}
-      auto issue_pv = [&](int t, int pe) -> bool {
-        const int sv = pe % L::kStagesV;
-        if (!mbar_wait_warp(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
-        if (!mbar_wait_warp(bar(L::bVFull + sv), (uint32_t)(pe / L::kStagesV) & 1u, ctl, 6)) return false;
+    regs_dec<kOtherRegs>();
+    for (;; ++kq) {
+      item_sync();
+      const int len = (int)misc[2];
+      // ------------------------------------------------------------ MMA issuer
+      // Fixed schedule over the union list: at entry e, for each Q tile t, first
+      // the pending O_t += P_t V of t's previous live entry (waiting for P_t),
+      // then S_t = Q_t K_e^T if t is live at e. For dense rows this is
+      //   PV0(e-1), S0(e), PV1(e-1), S1(e), PV0(e), ...
+      // so that while one softmax group works the tensor core runs the other
+      // tile's products. A pending PV is issued at the very next entry, so each
+      // V slot is released one entry after its load and the K slot of entry e
+      // right after its S products.
+      {   // the whole warp runs the schedule; one elected lane issues each MMA and commit
+        constexpr uint32_t idS = idesc_16<F16>(128, 128, false, false);
+        constexpr uint32_t idO = idesc_16<F16>(128, D, false, true);
+        const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+        const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+        // P_t: over S_t, or in columns of its own (after O_1)
+        const uint32_t tP[2] = {L::kOwnP ? tmem + 256u + 2u * D : tS[0], L::kOwnP ? tmem + 320u + 2u * D : tS[1]};
+        const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
+        const uint64_t dK0 = desc_kmajor(sbase + L::kK, 0);
+        const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
+        constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
+        int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
+        // the last entry live for each Q tile: its PV completes O_t, which the
+        // softmax group may then read out while the other tile's products run
+        const int lastE[2] = {(int)misc[4], (int)misc[5]};
+        uint32_t npv_item[2] = {0u, 0u};   // PV groups of this item per Q tile
+        bool ok = mbar_wait_warp(bar(L::bQFull), kq & 1u, ctl, 4);
         tc_fence_after();
-        const uint64_t dV = dV0 + (uint64_t)sv * kSlotStep;
-        const uint32_t acc0 = npv[t] > 0 ? 1u : 0u;
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts_w(tO[t], tP[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
-        if constexpr (L::kOwnP) mma_commit_w(bar(L::bPVDone + t));   // P_t may be rewritten, O_t rescaled
-        if (pe == lastE[t]) mma_commit_w(bar(L::bOFinal + t));       // O_t is complete
-        ++npv[t];
-        return true;
-      };
 
-      if constexpr (L::kOwnP) {
-        // Own P columns: at entry e, first S_t(e) for each live tile, each as
-        // soon as group t has read its previous S_t into registers, then the
-        // PVs of entry e - 1. For dense rows:
-        //   S0(e), S1(e), PV0(e-1), PV1(e-1), S0(e+1), ...
-        // so S_t(e+1) is computed while group t still works on S_t(e).
-        uint32_t ns[2] = {0u, 0u};   // S products issued per Q tile
-        for (int e = 0; e < len && ok; ++e) {
-          const uint32_t ent = list[e];
-          const int sk = e % L::kStagesK;
-          bool k_ready = false;
+        // O_t += P_t V_{entry pe}
+        auto issue_pv = [&](int t, int pe) -> bool {
+          const int nvp = eV + pe;
+          const int sv = nvp % L::kStagesV;
+          if (!mbar_wait_warp(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
+          if (!mbar_wait_warp(bar(L::bVFull + sv), (uint32_t)(nvp / L::kStagesV) & 1u, ctl, 6)) return false;
+          tc_fence_after();
+          const uint64_t dV = dV0 + (uint64_t)sv * kSlotStep;
+          const uint32_t acc0 = npv_item[t] > 0 ? 1u : 0u;
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok || !entry_live(ent, t)) continue;
-            if (ns[t] > 0 && !(ok = mbar_wait_warp(bar(L::bSFree + t), (ns[t] - 1u) & 1u, ctl, 8))) break;
-            if (!k_ready) {
-              ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            const uint64_t dK = dK0 + (uint64_t)sk * kSlotStep;
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ts_w(tO[t], tP[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
+          if constexpr (L::kOwnP) mma_commit_w(bar(L::bPVDone + t));   // P_t may be rewritten, O_t rescaled
+          if (pe == lastE[t]) mma_commit_w(bar(L::bOFinal + t));       // O_t is complete
+          ++npv[t];
+          ++npv_item[t];
+          return true;
+        };
+
+        if constexpr (L::kOwnP) {
+          // Own P columns: at entry e, first S_t(e) for each live tile, each as
+          // soon as group t has read its previous S_t into registers, then the
+          // PVs of entry e - 1. For dense rows:
+          //   S0(e), S1(e), PV0(e-1), PV1(e-1), S0(e+1), ...
+          // so S_t(e+1) is computed while group t still works on S_t(e).
+          for (int e = 0; e < len && ok; ++e) {
+            const uint32_t ent = list[e];
+            const int sk = (eK + e) % L::kStagesK;
+            bool k_ready = false;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_ss_w(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
-            mma_commit_w(bar(L::bSFull + t));
-            ++ns[t];
-          }
-          if (!ok) break;
-          mma_commit_w(bar(L::bKEmpty + sk));   // K_e is no longer needed
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
-            prev[t] = entry_live(ent, t) ? e : -1;
-          }
-          if (!ok) break;
-          if (e > 0) mma_commit_w(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
-        }
-      } else {
-        for (int e = 0; e < len && ok; ++e) {
-          const uint32_t ent = list[e];
-          const int sk = e % L::kStagesK;
-          bool k_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!ok) break;
-            if (prev[t] >= 0) {
-              ok = issue_pv(t, prev[t]);
-              prev[t] = -1;
-              if (!ok) break;
-            }
-            if (entry_live(ent, t)) {
+            for (int t = 0; t < 2; ++t) {
+              if (!ok || !entry_live(ent, t)) continue;
+              if (ns[t] > 0 && !(ok = mbar_wait_warp(bar(L::bSFree + t), (ns[t] - 1u) & 1u, ctl, 8))) break;
               if (!k_ready) {
-                ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)(e / L::kStagesK) & 1u, ctl, 7);
+                ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)((eK + e) / L::kStagesK) & 1u, ctl, 7);
                 if (!ok) break;
                 tc_fence_after();
                 k_ready = true;
@@ -355,229 +400,294 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               for (int ks = 0; ks < D / 16; ++ks)
                 mma_ss_w(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
               mma_commit_w(bar(L::bSFull + t));
-              prev[t] = e;
+              ++ns[t];
+            }
+            if (!ok) break;
+            mma_commit_w(bar(L::bKEmpty + sk));   // K_e is no longer needed
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);
+              prev[t] = entry_live(ent, t) ? e : -1;
+            }
+            if (!ok) break;
+            if (e > 0) mma_commit_w(bar(L::bVEmpty + (eV + e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
+          }
+        } else {
+          for (int e = 0; e < len && ok; ++e) {
+            const uint32_t ent = list[e];
+            const int sk = (eK + e) % L::kStagesK;
+            bool k_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (!ok) break;
+              if (prev[t] >= 0) {
+                ok = issue_pv(t, prev[t]);
+                prev[t] = -1;
+                if (!ok) break;
+              }
+              if (entry_live(ent, t)) {
+                if (!k_ready) {
+                  ok = mbar_wait_warp(bar(L::bKFull + sk), (uint32_t)((eK + e) / L::kStagesK) & 1u, ctl, 7);
+                  if (!ok) break;
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                const uint64_t dK = dK0 + (uint64_t)sk * kSlotStep;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                  mma_ss_w(tS[t], dQ[t] + kmajor_step(ks), dK + kmajor_step(ks), idS, ks > 0 ? 1u : 0u);
+                mma_commit_w(bar(L::bSFull + t));
+                prev[t] = e;
+              }
+            }
+            if (!ok) break;
+            mma_commit_w(bar(L::bKEmpty + sk));                       // K_e is no longer needed
+            if (e > 0) mma_commit_w(bar(L::bVEmpty + (eV + e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
+          }
+        }
+        if (ok) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);   // (commits O_t's completion)
+          }
+          // the last entry's V slot goes back to the producer
+          if (ok && len > 0) mma_commit_w(bar(L::bVEmpty + (eV + len - 1) % L::kStagesV));
+        }
+      }
+      item_sync();
+      item = next_item();
+      if (item < 0) break;
+      eK += len;
+      eV += len;
+    }
+    // every MMA issued has completed before TMEM is freed
+    mma_commit_w(bar(L::bDrain));
+    drain_wait(bar(L::bDrain), 0);
+  } else if (warp < 8) {
+    regs_inc<kSoftmaxRegs>();
+    for (;; ++kq) {
+      int bh = 0;
+      const int c = nC - 1 - split_grouped(item, p.group, nC, BH, &bh);
+      const int qi0 = 2 * c;
+      const int kvl = effective_kv_len(p.kv_len, bh / p.H, p.N);
+      item_sync();
+      const int len = (int)misc[2];
+      // ------------------------------------------------------------ softmax groups
+      const int t = warp >> 2;                 // Q tile of this warpgroup
+      const int r = tid & 127;                 // row within the tile = TMEM lane
+      const int qi = qi0 + t;
+      const int row = kTile * qi + r;          // query index within the head
+      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_off;
+      const uint32_t tO = tmem + 256u + (uint32_t)(t * D) + lane_off;
+      const uint32_t tP = L::kOwnP ? tmem + 256u + 2u * D + 64u * (uint32_t)t + lane_off : tS;
+      const float sl2 = p.scale_log2;
+
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      uint32_t n = 0;   // S tiles of this item (nS: of all items)
+      bool ok = (qi < p.nT);
+      for (int e = 0; e < len && ok; ++e) {
+        const uint32_t ent = list[e];
+        if (!entry_live(ent, t)) continue;
+        if (!mbar_wait_warp(bar(L::bSFull + t), nS & 1u, ctl, 10 + t)) { ok = false; break; }
+        tc_fence_after();
+        if (p.chk.rec != nullptr && r == 0) {   // the tile as this kernel computes it
+          uint8_t* rc = p.chk.rec + ((size_t)bh * p.nT + qi) * p.nT + entry_j(ent);
+          *rc = (uint8_t)(*rc + (entry_partial(ent, t) ? 2 : 1));
+        }
+        float x[128];
+        {
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          tmem_ld32(tS + 0u, u0);
+          tmem_ld32(tS + 32u, u1);
+          tmem_ld32(tS + 64u, u2);
+          tmem_ld32(tS + 96u, u3);
+          tmem_ld_wait(u0);
+          tmem_ld_wait(u1);
+          tmem_ld_wait(u2);
+          tmem_ld_wait(u3);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(u0[i]);
+            x[32 + i] = __uint_as_float(u1[i]);
+            x[64 + i] = __uint_as_float(u2[i]);
+            x[96 + i] = __uint_as_float(u3[i]);
+          }
+        }
+        if constexpr (L::kOwnP) {   // S_t is in registers: the next S_t may be computed
+          tc_fence_before();
+          mbar_arrive_warp(bar(L::bSFree + t));
+        }
+        if (entry_partial(ent, t)) {
+          const int key0 = kTile * entry_j(ent);
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            const int key = key0 + i;
+            if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
+          }
+        }
+        // row max with three-input max: 8 independent chains over 128 scores
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < 120; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], x[i + k], x[i + 8 + k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[120 + k]);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float m_new = mx * sl2;
+        // move the reference max only when the row max grew by more than the
+        // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
+        // warp rescales when any of its rows needs it (alpha = 1 for the rest)
+        const bool move = (n == 0) || (m_new > m_ref + kRescaleThreshold);
+        float alpha = 1.f;
+        if (move) {
+          alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+        }
+        if (L::kOwnP && nS > 0) {
+          // the previous O_t += P_t V has completed (of this item or the last
+          // one): O_t may be rescaled and the P_t columns rewritten
+          if (!mbar_wait_warp(bar(L::bPVDone + t), (nS - 1u) & 1u, ctl, 16 + t)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
+          uint32_t u[32];
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            tmem_ld32(tO + 32u * cc, u);
+            tmem_ld_wait(u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(tO + 32u * cc, u);
+          }
+          tmem_st_wait();
+        }
+        const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // packed fp32 pairs (one f32x2 instruction per two keys) for the
+        // exponent arguments and the row sum: the softmax is issue-bound
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 nref2 = make_float2(-ref, -ref);
+        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
+        // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
+        // four rows of a lane quad share their calls: for every 16 keys each
+        // lane makes the call of one 4-key block and a transpose across the
+        // quad hands every row its word of all four (one call per 16 keys and
+        // row instead of four)
+        const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
+        uint32_t kw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 a = __ffma2_rn(make_float2(x[64 * hh + 2 * i], x[64 * hh + 2 * i + 1]), sl2x2, nref2);
+            const float p0 = ex2(a.x);
+            const float p1 = ex2(a.y);
+            sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
+            if constexpr (DROP) {
+              if ((i & 7) == 0) {
+                const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
+                                              (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
+                kw[0] = v.x;
+                kw[1] = v.y;
+                kw[2] = v.z;
+                kw[3] = v.w;
+                quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
+              }
+              const uint32_t rw = kw[(i >> 1) & 3];
+              const uint32_t sh = 16u * (uint32_t)(i & 1);
+              const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
+              const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
+              pk[i] = pack2<F16>(d0, d1);
+            } else {
+              pk[i] = pack2<F16>(p0, p1);
             }
           }
-          if (!ok) break;
-          mma_commit_w(bar(L::bKEmpty + sk));                       // K_e is no longer needed
-          if (e > 0) mma_commit_w(bar(L::bVEmpty + (e - 1) % L::kStagesV));   // both PVs of entry e-1 issued
-        }
-      }
-      if (ok) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (ok && prev[t] >= 0) ok = issue_pv(t, prev[t]);   // (commits O_t's completion)
-        }
-      }
-      // every MMA this warp issued must be complete before TMEM is freed
-      mma_commit_w(bar(L::bDrain));
-      drain_wait(bar(L::bDrain), 0);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax groups
-    regs_inc<kSoftmaxRegs>();
-    const int t = warp >> 2;                 // Q tile of this warpgroup
-    const int r = tid & 127;                 // row within the tile = TMEM lane
-    const int qi = qi0 + t;
-    const int row = kTile * qi + r;          // query index within the head
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + (uint32_t)(t * 128) + lane_off;
-    const uint32_t tO = tmem + 256u + (uint32_t)(t * D) + lane_off;
-    const uint32_t tP = L::kOwnP ? tmem + 256u + 2u * D + 64u * (uint32_t)t + lane_off : tS;
-    const float sl2 = p.scale_log2;
-
-    float m_ref = -INFINITY;
-    float l = 0.f;
-    uint32_t n = 0;
-    bool ok = (qi < p.nT);
-    for (int e = 0; e < len && ok; ++e) {
-      const uint32_t ent = list[e];
-      if (!entry_live(ent, t)) continue;
-      if (!mbar_wait_warp(bar(L::bSFull + t), n & 1u, ctl, 10 + t)) { ok = false; break; }
-      tc_fence_after();
-      if (p.chk.rec != nullptr && r == 0) {   // the tile as this kernel computes it
-        uint8_t* rc = p.chk.rec + ((size_t)bh * p.nT + qi) * p.nT + entry_j(ent);
-        *rc = (uint8_t)(*rc + (entry_partial(ent, t) ? 2 : 1));
-      }
-      float x[128];
-      {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
-        tmem_ld32(tS + 0u, u0);
-        tmem_ld32(tS + 32u, u1);
-        tmem_ld32(tS + 64u, u2);
-        tmem_ld32(tS + 96u, u3);
-        tmem_ld_wait(u0);
-        tmem_ld_wait(u1);
-        tmem_ld_wait(u2);
-        tmem_ld_wait(u3);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(u0[i]);
-          x[32 + i] = __uint_as_float(u1[i]);
-          x[64 + i] = __uint_as_float(u2[i]);
-          x[96 + i] = __uint_as_float(u3[i]);
-        }
-      }
-      if constexpr (L::kOwnP) {   // S_t is in registers: the next S_t may be computed
-        tc_fence_before();
-        mbar_arrive_warp(bar(L::bSFree + t));
-      }
-      if (entry_partial(ent, t)) {
-        const int key0 = kTile * entry_j(ent);
-#pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const int key = key0 + i;
-          if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
-        }
-      }
-      // row max with three-input max: 8 independent chains over 128 scores
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = x[k];
-#pragma unroll
-      for (int i = 8; i < 120; i += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], x[i + k], x[i + 8 + k]);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[120 + k]);
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      const float m_new = mx * sl2;
-      // move the reference max only when the row max grew by more than the
-      // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
-      // warp rescales when any of its rows needs it (alpha = 1 for the rest)
-      const bool move = (n == 0) || (m_new > m_ref + kRescaleThreshold);
-      float alpha = 1.f;
-      if (move) {
-        alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
-        l *= alpha;
-        m_ref = m_new;
-      }
-      if (L::kOwnP && n > 0) {
-        // the previous O_t += P_t V has completed: O_t may be rescaled and
-        // the P_t columns rewritten
-        if (!mbar_wait_warp(bar(L::bPVDone + t), (n - 1u) & 1u, ctl, 16 + t)) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
-        uint32_t u[32];
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          tmem_ld32(tO + 32u * cc, u);
-          tmem_ld_wait(u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(tO + 32u * cc, u);
+          tmem_st32(tP + 32u * hh, pk);
         }
         tmem_st_wait();
+        const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        l += s4.x + s4.y;
+        tc_fence_before();
+        mbar_arrive_warp(bar(L::bPFull + t));
+        ++n;
+        ++nS;
       }
-      const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // packed fp32 pairs (one f32x2 instruction per two keys) for the
-      // exponent arguments and the row sum: the softmax is issue-bound
-      const float2 sl2x2 = make_float2(sl2, sl2);
-      const float2 nref2 = make_float2(-ref, -ref);
-      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
-      // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
-      // four rows of a lane quad share their calls: for every 16 keys each
-      // lane makes the call of one 4-key block and a transpose across the
-      // quad hands every row its word of all four (one call per 16 keys and
-      // row instead of four)
-      const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
-      uint32_t kw[4] = {0u, 0u, 0u, 0u};
+
+      if (qi < p.nT) {
+        // all MMAs that read Q_t have completed (or never ran); make sure the
+        // Q load itself has landed before its buffer is reused for staging O
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) ok = mbar_wait_warp(bar(L::bQFull), kq & 1u, ctl, 12 + t);
+        if (ok && n > 0) ok = mbar_wait_warp(bar(L::bOFinal + t), nOF & 1u, ctl, 14 + t);
+        if (n > 0) ++nOF;
+        if (!ok) drain_wait(bar(L::bQFull), kq & 1u);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
+        tc_fence_after();
+        uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
+        const float inv_l = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const bool have_o = ok && n > 0;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 a = __ffma2_rn(make_float2(x[64 * hh + 2 * i], x[64 * hh + 2 * i + 1]), sl2x2, nref2);
-          const float p0 = ex2(a.x);
-          const float p1 = ex2(a.y);
-          sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
-          if constexpr (DROP) {
-            if ((i & 7) == 0) {
-              const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
-                                            (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
-              kw[0] = v.x;
-              kw[1] = v.y;
-              kw[2] = v.z;
-              kw[3] = v.w;
-              quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
-            }
-            const uint32_t rw = kw[(i >> 1) & 3];
-            const uint32_t sh = 16u * (uint32_t)(i & 1);
-            const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
-            const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
-            pk[i] = pack2<F16>(d0, d1);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          if (have_o) {
+            tmem_ld32(tO + 32u * cc, u);
+            tmem_ld_wait(u);
           } else {
-            pk[i] = pack2<F16>(p0, p1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) u[i] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<F16>(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
+          // 32 columns = 4 chunks of 16 bytes, 128B-swizzled rows
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int col = 32 * cc + 8 * k;           // first column of the chunk
+            const int h = col >> 6;                    // 64-column half
+            const int chunk = (col & 63) >> 3;         // chunk within the 128-byte row
+            uint8_t* dst = stage + h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
           }
         }
-        tmem_st32(tP + 32u * hh, pk);
+        if (row < p.N) {
+          float lse = -INFINITY;
+          if (have_o && l > 0.f) lse = (m_ref + log2f(l)) * 0.69314718055994531f;
+          p.lse[(size_t)bh * p.N + row] = lse;
+        }
+        // each warp stores its own 32 rows (boxes of 32 rows), so that no warp
+        // ever waits for another at a group-wide barrier
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = kTile * qi + 32 * (warp & 3);
+          if (row0 < p.N)
+            for (int h = 0; h < L::kHalves; ++h)
+              tma_store_3d(&to, smem_u32(stage) + h * 16384 + 4096 * (warp & 3), 64 * h, row0, bh);
+          bulk_commit_group();
+          bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
+        }
       }
-      tmem_st_wait();
-      const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
-      const float2 s4 = __fadd2_rn(s01, s23);
-      l += s4.x + s4.y;
-      tc_fence_before();
-      mbar_arrive_warp(bar(L::bPFull + t));
-      ++n;
+      item_sync();
+      item = next_item();
+      if (item < 0) break;
     }
-
-    if (qi < p.nT) {
-      // all MMAs that read Q_t have completed (or never ran); make sure the
-      // Q load itself has landed before its buffer is reused for staging O
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (ok) ok = mbar_wait_warp(bar(L::bQFull), 0, ctl, 12 + t);
-      if (ok && n > 0) ok = mbar_wait_warp(bar(L::bOFinal + t), 0, ctl, 14 + t);
-      if (!ok) drain_wait(bar(L::bQFull), 0);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
-      tc_fence_after();
-      uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
-      const float inv_l = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
-      const bool have_o = ok && n > 0;
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
-        if (have_o) {
-          tmem_ld32(tO + 32u * cc, u);
-          tmem_ld_wait(u);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<F16>(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
-        // 32 columns = 4 chunks of 16 bytes, 128B-swizzled rows
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int col = 32 * cc + 8 * k;           // first column of the chunk
-          const int h = col >> 6;                    // 64-column half
-          const int chunk = (col & 63) >> 3;         // chunk within the 128-byte row
-          uint8_t* dst = stage + h * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
-      }
-      if (row < p.N) {
-        float lse = -INFINITY;
-        if (have_o && l > 0.f) lse = (m_ref + log2f(l)) * 0.69314718055994531f;
-        p.lse[(size_t)bh * p.N + row] = lse;
-      }
-      // each warp stores its own 32 rows (boxes of 32 rows), so that no warp
-      // ever waits for another at a group-wide barrier
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int row0 = kTile * qi + 32 * (warp & 3);
-        if (row0 < p.N)
-          for (int h = 0; h < L::kHalves; ++h)
-            tma_store_3d(&to, smem_u32(stage) + h * 16384 + 4096 * (warp & 3), 64 * h, row0, bh);
-        bulk_commit_group();
-        bulk_wait_group_read_all();   // the store has read the staging; the grid's end makes it visible
-      }
+  } else {
+    regs_dec<kOtherRegs>();   // warp 11: no role of its own, it only keeps the item barriers
+    for (;; ++kq) {
+      item_sync();
+      item_sync();
+      item = next_item();
+      if (item < 0) break;
     }
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {

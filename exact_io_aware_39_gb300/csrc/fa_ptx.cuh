@@ -230,6 +230,32 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ---------------------------------------------------------------------------
+// Cluster launch control: a running CTA cancels a CTA of its own grid that
+// has not started yet and takes over its work. The 16-byte answer is written
+// into shared memory and completes a transaction count on the mbarrier.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void clc_try_cancel(uint32_t answer_smem, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               :: "r"(answer_smem), "r"(bar) : "memory");
+}
+
+// x index of the first CTA the answer cancelled, or -1 when nothing was left
+// to cancel (read after the mbarrier phase has completed).
+__device__ __forceinline__ int clc_first_ctaid_x(uint32_t answer_smem) {
+  uint32_t x, ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 h;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "mov.u32 %0, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, h;\n\t}"
+      : "=r"(x), "=r"(ok) : "r"(answer_smem) : "memory");
+  return ok ? (int)x : -1;
+}
+
+// ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation tensor core
 // ---------------------------------------------------------------------------
 

@@ -57,7 +57,8 @@ typedef enum {
   FA_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small */
   FA_ERR_CUDA = 4,             /* a CUDA runtime call or a launch failed */
   FA_ERR_DEVICE_TIMEOUT = 5,   /* a kernel's bounded wait ran out (device error word) */
-  FA_ERR_DEVICE_INTERNAL = 6,  /* a kernel found its shared memory misaligned */
+  FA_ERR_DEVICE_INTERNAL = 6,  /* a kernel found an internal inconsistency (misaligned shared memory,
+                                  a work item out of range) */
   FA_ERR_SCRATCH_LIMIT = 7     /* flash_attn_bwd_noalloc: shape needs more than its fixed scratch */
 } fa_status;
 
