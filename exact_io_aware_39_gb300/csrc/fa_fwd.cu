@@ -10,24 +10,30 @@
 // chip (milestone page, "The idea -- Recomputation").
 //
 // GB300 design (not the pages' A100 design):
-//   * one CTA owns two 128-row Q tiles of one (batch, head); 12 warps:
+//   * a work item is a pair of 128-row Q tiles of one (batch, head); a CTA
+//     (one per SM) takes items one after another: its own, then CTAs of the
+//     grid that have not started, cancelled through cluster launch control;
+//     12 warps:
 //       warps 0-3  softmax / correction / epilogue of Q tile 0 (TMEM lanes 0-127)
 //       warps 4-7  the same for Q tile 1
-//       warp  8    TMA producer of Q (once) and of the K ring
-//       warp  9    TMEM allocator and the single thread that issues tcgen05.mma
+//       warp  8    builds each item's list of live key tiles; TMA producer of
+//                  Q and of the K ring; asks for the next item
+//       warp  9    TMEM allocator; runs the MMA schedule (one lane picked by
+//                  elect.sync issues each tcgen05.mma)
 //       warp 10    TMA producer of the V ring
-//       warp 11    idle; the third warpgroup gives its registers to the
+//       warp 11    no role; the third warpgroup gives its registers to the
 //                  softmax warpgroups (216 vs 72 per thread)
 //   * S_t = Q_t K_j^T accumulates in TMEM (128 fp32 columns per Q tile); the
-//     softmax warps overwrite it in place with P_t as packed bf16, which the
-//     tensor core then reads straight from TMEM for O_t += P_t V_j;
-//   * O_t accumulates in TMEM for the whole K/V sweep and is written once;
-//   * the two Q tiles ping-pong: while one softmax group works on its S, the
-//     tensor core runs the other tile's P V and next S;
-//   * the MMA thread follows a fixed schedule over the union list of key
+//     softmax warps write P_t as packed bf16 (over S_t at d = 128, into
+//     columns of their own at d = 64), which the tensor core then reads
+//     straight from TMEM for O_t += P_t V_j;
+//   * O_t accumulates in TMEM over the item's K/V sweep and is written once;
+//   * the two Q tiles share the tensor core: while one softmax group works on
+//     its S, the tensor core runs the other tile's P V and next S;
+//   * the MMA warp follows a fixed schedule over the union list of key
 //     tiles live for either Q tile (causal, key-length and block-sparse
 //     skipping are exact per tile), while K/V tiles are loaded once for the
-//     pair.
+//     pair;
 //   * the running max is moved (and O rescaled) only when a new row max
 //     exceeds it by more than 2^8; the final O / l and LSE use the same
 //     reference max, so the result is unchanged.
