@@ -51,6 +51,7 @@ constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 regi
 constexpr int kOtherRegs = 72;
 constexpr int kListMax = kMaxN / kTile;   // union list capacity
 constexpr float kRescaleThreshold = 8.0f; // log2 units
+constexpr float kSpecSumLimit = 256.0f;    // 2^kRescaleThreshold
 
 template <int D>
 struct FwdLayout {
@@ -533,94 +534,111 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
           }
         }
-        // row max with three-input max: 8 independent chains over 128 scores
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
-#pragma unroll
-        for (int i = 8; i < 120; i += 16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], x[i + k], x[i + 8 + k]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[120 + k]);
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-        const float m_new = mx * sl2;
-        // move the reference max only when the row max grew by more than the
-        // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
-        // warp rescales when any of its rows needs it (alpha = 1 for the rest)
-        const bool move = (n == 0) || (m_new > m_ref + kRescaleThreshold);
-        float alpha = 1.f;
-        if (move) {
-          alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
-          l *= alpha;
-          m_ref = m_new;
-        }
         if (L::kOwnP && nS > 0) {
           // the previous O_t += P_t V has completed (of this item or the last
           // one): O_t may be rescaled and the P_t columns rewritten
           if (!mbar_wait_warp(bar(L::bPVDone + t), (nS - 1u) & 1u, ctl, 16 + t)) { ok = false; break; }
           tc_fence_after();
         }
-        if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
-          uint32_t u[32];
+        // Two passes at most. Pass 0 (not for a row block's first tile) takes the
+        // exponentials with the current reference max: if every row of the warp
+        // then sums to less than 2^8, no score exceeds the reference by the
+        // rescale threshold, so the row max would not have moved it and P is
+        // exactly what pass 1 would give. Otherwise pass 1 takes the row max,
+        // moves the reference (rescaling O) where it grew past the threshold,
+        // and redoes the exponentials (the whole warp: the TMEM stores are
+        // warp-collective). This saves the row max on most tiles.
+        float s_row = 0.f;
+        for (int pass = (n == 0 || DROP) ? 1 : 0; pass < 2; ++pass) {   // (with dropout: always the row max)
+          if (pass == 1) {
+            // row max with three-input max: 8 independent chains over 128 scores
+            float mx8[8];
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            tmem_ld32(tO + 32u * cc, u);
-            tmem_ld_wait(u);
+            for (int k = 0; k < 8; ++k) mx8[k] = x[k];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(tO + 32u * cc, u);
-          }
-          tmem_st_wait();
-        }
-        const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // packed fp32 pairs (one f32x2 instruction per two keys) for the
-        // exponent arguments and the row sum: the softmax is issue-bound
-        const float2 sl2x2 = make_float2(sl2, sl2);
-        const float2 nref2 = make_float2(-ref, -ref);
-        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
-        // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
-        // four rows of a lane quad share their calls: for every 16 keys each
-        // lane makes the call of one 4-key block and a transpose across the
-        // quad hands every row its word of all four (one call per 16 keys and
-        // row instead of four)
-        const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
-        uint32_t kw[4] = {0u, 0u, 0u, 0u};
+            for (int i = 8; i < 120; i += 16)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[32];
+              for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], x[i + k], x[i + 8 + k]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 a = __ffma2_rn(make_float2(x[64 * hh + 2 * i], x[64 * hh + 2 * i + 1]), sl2x2, nref2);
-            const float p0 = ex2(a.x);
-            const float p1 = ex2(a.y);
-            sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
-            if constexpr (DROP) {
-              if ((i & 7) == 0) {
-                const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
-                                              (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
-                kw[0] = v.x;
-                kw[1] = v.y;
-                kw[2] = v.z;
-                kw[3] = v.w;
-                quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
+            for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[120 + k]);
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+            const float m_new = mx * sl2;
+            // move the reference max only when the row max grew by more than the
+            // threshold; the O rescale is warp-collective (tcgen05.ld/st), so a
+            // warp rescales when any of its rows needs it (alpha = 1 for the rest)
+            const bool move = (n == 0) || (m_new > m_ref + kRescaleThreshold);
+            float alpha = 1.f;
+            if (move) {
+              alpha = (n == 0 || m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+              l *= alpha;
+              m_ref = m_new;
+            }
+            if (n > 0 && __any_sync(0xFFFFFFFFu, move)) {
+              uint32_t u[32];
+#pragma unroll
+              for (int cc = 0; cc < D / 32; ++cc) {
+                tmem_ld32(tO + 32u * cc, u);
+                tmem_ld_wait(u);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                tmem_st32(tO + 32u * cc, u);
               }
-              const uint32_t rw = kw[(i >> 1) & 3];
-              const uint32_t sh = 16u * (uint32_t)(i & 1);
-              const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
-              const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
-              pk[i] = pack2<F16>(d0, d1);
-            } else {
-              pk[i] = pack2<F16>(p0, p1);
+              tmem_st_wait();
             }
           }
-          tmem_st32(tP + 32u * hh, pk);
+          const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // packed fp32 pairs (one f32x2 instruction per two keys) for the
+          // exponent arguments and the row sum: the softmax is issue-bound
+          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 nref2 = make_float2(-ref, -ref);
+          float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
+          // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
+          // four rows of a lane quad share their calls: for every 16 keys each
+          // lane makes the call of one 4-key block and a transpose across the
+          // quad hands every row its word of all four (one call per 16 keys and
+          // row instead of four)
+          const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
+          uint32_t kw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 a = __ffma2_rn(make_float2(x[64 * hh + 2 * i], x[64 * hh + 2 * i + 1]), sl2x2, nref2);
+              const float p0 = ex2(a.x);
+              const float p1 = ex2(a.y);
+              sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
+              if constexpr (DROP) {
+                if ((i & 7) == 0) {
+                  const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
+                                                (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
+                  kw[0] = v.x;
+                  kw[1] = v.y;
+                  kw[2] = v.z;
+                  kw[3] = v.w;
+                  quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
+                }
+                const uint32_t rw = kw[(i >> 1) & 3];
+                const uint32_t sh = 16u * (uint32_t)(i & 1);
+                const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
+                const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
+                pk[i] = pack2<F16>(d0, d1);
+              } else {
+                pk[i] = pack2<F16>(p0, p1);
+              }
+            }
+            tmem_st32(tP + 32u * hh, pk);
+          }
+          tmem_st_wait();
+          const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
+          const float2 s4 = __fadd2_rn(s01, s23);
+          s_row = s4.x + s4.y;
+          // (a row whose reference is still -inf, every earlier key masked,
+          // always takes the row max)
+          if (pass == 0 && __all_sync(0xFFFFFFFFu, s_row < kSpecSumLimit && m_ref != -INFINITY)) break;
         }
-        tmem_st_wait();
-        const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
-        const float2 s4 = __fadd2_rn(s01, s23);
-        l += s4.x + s4.y;
+        l += s_row;
         tc_fence_before();
         mbar_arrive_warp(bar(L::bPFull + t));
         ++n;
