@@ -53,13 +53,32 @@ namespace fa {
 
 namespace {
 
-constexpr int kBwdThreads = 512;
-// per-thread registers after reallocation: 128 x (160 + 160 + 96 + 96) = 512 x 128
-constexpr int kComputeRegs = 160;
-constexpr int kDrainRegs = 96;
-constexpr int kOtherRegs = 96;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+// Warp roles of the main kernel. kGroups P/dS warpgroups split each tile's
+// 128 query columns (kCols each), then one warpgroup drains dQ and one holds
+// the TMA producer, the MMA warp and two idle warps. Four groups of 32
+// queries only at d = 128 with dropout, where the keep bits (Philox rounds)
+// make the P/dS work the bound (measured: backward main +8 % there, -6 %
+// without dropout, where two groups with more registers each run ahead of
+// the tensor pipe by less). The registers after
+// reallocation add up to what the CTA is launched with (setmaxnreg.inc
+// draws on that, not on the SM): 2 groups, 512 threads launched at 128:
+// 2 x 128 x 160 + 128 x 96 + 128 x 96 = 512 x 128; 4 groups, 768 threads
+// launched at 80: 4 x 128 x 88 + 128 x 72 + 128 x 56 = 768 x 80.
+template <int D, bool DROP>
+struct BwdWarps {
+  static constexpr int kGroups = (D == 128 && DROP) ? 4 : 2;
+  static constexpr int kCols = kTile / kGroups;
+  static constexpr int kThreads = 128 * (kGroups + 2);
+  static constexpr int kDrainWarp0 = 4 * kGroups;
+  static constexpr int kProducerWarp = kDrainWarp0 + 4;
+  static constexpr int kMmaWarp = kProducerWarp + 1;
+  static constexpr int kComputeRegs = kGroups == 2 ? 160 : 88;
+  static constexpr int kDrainRegs = kGroups == 2 ? 96 : 72;
+  static constexpr int kOtherRegs = kGroups == 2 ? 96 : 56;
+  static_assert(128 * (kGroups * kComputeRegs + kDrainRegs + kOtherRegs) ==
+                    kThreads * (kGroups == 2 ? 128 : 80),
+                "the reallocated registers must add up to the launch allocation");
+};
 
 template <int D>
 struct BwdLayout {
@@ -93,7 +112,7 @@ struct BwdLayout {
   // work items reach the other roles through a ring filled by the producer
   static constexpr int kItemRing = 4;
   static constexpr int bItemFull = bKVFree + kKV;            // [kItemRing]
-  static constexpr int bItemEmpty = bItemFull + kItemRing;   // [kItemRing]: MMA thread + 8 compute + 4 drain warps
+  static constexpr int bItemEmpty = bItemFull + kItemRing;   // [kItemRing]: MMA warp, compute and drain warps
   static constexpr int bdSHalf = bItemEmpty + kItemRing;     // the first 32 dS^T columns of each warpgroup
   static constexpr int kNumBars = bdSHalf + 1;
   static constexpr int kMisc = kBar + 8 * kNumBars;   // tmem slot, abort flag, -, wait limit
@@ -115,12 +134,13 @@ __device__ __forceinline__ uint32_t swz_off(int r, int col) {
 }
 
 template <int D, bool F16, bool DROP>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdWarps<D, DROP>::kThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                    const __grid_constant__ CUtensorMap tdq, const BwdParams p, const float scale) {
   using L = BwdLayout<D>;
+  using W = BwdWarps<D, DROP>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
@@ -185,16 +205,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdSHalf) ? 8u
+      mbar_init(bar(i), (i == L::bPFull || i == L::bdSFull || i == L::bdSHalf) ? (uint32_t)(4 * W::kGroups)
                         : i == L::bdQFree ? 4u                                       // the four drain warps
-                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? 2u         // one thread per compute group
+                        : (i >= L::bKVFree && i < L::bKVFree + L::kKV) ? (uint32_t)W::kGroups   // one thread per compute group
                         : (!L::kGroupDrain && i >= L::bdOFree && i < L::bdOFree + L::kStages) ? 4u   // the drain warps
-                        : i >= L::bItemEmpty ? 13u : 1u);   // arrivals
+                        : (i >= L::bItemEmpty && i < L::bItemEmpty + L::kItemRing)
+                            ? (uint32_t)(1 + 4 * W::kGroups + 4) : 1u);   // arrivals: MMA, compute and drain warps
     abort_flag[0] = 0u;
     abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == W::kMmaWarp) {
     tmem_alloc(smem_u32(misc), 512);
     tmem_relinquish();
   }
@@ -215,18 +236,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // which allows a schedule where nothing waits for its drain (see the MMA
   // issuer); at d = 128 it reuses the dP^T columns.
   constexpr bool kOwnDQ = (D == 64);
-  constexpr bool kSplitDS = (D == 128);   // dS^T handed to dK in two halves
+  constexpr bool kSplitDS = (D == 128) && W::kGroups == 2;   // dS^T handed to dK in two halves
   const uint32_t tQ = kOwnDQ ? tmem + 2u * D + 256u : tP;
   // dS^T for dK: packed into the S columns next to P^T at d = 128 (S^T of the
   // next tile is issued after dK), into the dP^T columns at d = 64 (S^T of
   // the next tile is issued before dK)
-  const uint32_t tDS = kOwnDQ ? tP : tS + 32u;
+  const uint32_t tDS = kOwnDQ ? tP : tS + (uint32_t)(W::kCols / 2);
+  // TMEM column of K step ks (16 queries) of the packed P^T / dS^T: each
+  // warpgroup packs its kCols queries into the first kCols / 2 of its own
+  // kCols S (or dP^T) columns
+  auto packed_col = [](int ks) -> uint32_t {
+    constexpr int kSteps = W::kCols / 16;   // K steps per warpgroup
+    return (uint32_t)(W::kCols * (ks / kSteps) + 8 * (ks % kSteps));
+  };
 
   // Every role walks the same items in the same order and counts the live
   // query tiles it has passed over all of them (g): ring slots and barrier
   // phases follow g, so the pipeline runs on across item boundaries.
-  if (warp >= 12) regs_dec<kOtherRegs>();
-  if (warp == kProducerWarp) {
+  if (warp >= W::kProducerWarp) regs_dec<W::kOtherRegs>();
+  if (warp == W::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&tq);
@@ -307,7 +335,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (s < nd) drain_wait(bar(L::bdOFull + s), (uint32_t)((nd - 1 - s) / L::kStages) & 1u);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == W::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // At d = 128 the whole warp runs the schedule and one elected lane issues
     // each MMA and commit; at d = 64 one lane runs it (measured: the warp-wide
@@ -368,16 +396,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const uint64_t mdO = desc_mnmajor(sdO, 0);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
-            // P of queries 0-63 packed in S columns 0-31, of queries 64-127 in 64-95
-            mma_ts_t<kW>(tdV, tS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mdO + mnmajor_step(ks), idV,
+            // P of each warpgroup's queries packed in the first half of its own S columns
+            mma_ts_t<kW>(tdV, tS + packed_col(ks), mdO + mnmajor_step(ks), idV,
                    (it > 0 || ks > 0) ? 1u : 0u);
           // next S^T of this item: at d = 64 right behind dV (the tensor pipe
           // runs in issue order, so dV has read P first), so that P of the
           // next tile is recomputed while dK, dQ and the next dP run; at
           // d = 128 after dQ, which leaves the next Q load the longest window
           if (kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
-          // dK += dS^T Q ; dQ_i = dS K. dS^T of queries 0-63 is in columns
-          // tDS + 0..31, of queries 64-127 in tDS + 64..95. At d = 128 each
+          // dK += dS^T Q ; dQ_i = dS K. dS^T is packed like P (packed_col) from
+          // tDS on; with two warpgroups, at d = 128 each
           // warpgroup hands over its first 32 queries (K steps 0, 1 and 4, 5)
           // before the rest (2, 3 and 6, 7), so half of dK runs while dS is
           // finished (measured: +1.5 % at d = 128, -0.4 to -1.2 % at d = 64)
@@ -390,7 +418,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
             for (int k4 = 0; k4 < (kSplitDS ? 4 : 8); ++k4) {
               const int ks = kSplitDS ? 2 * half + (k4 & 1) + 4 * (k4 >> 1) : k4;
-              mma_ts_t<kW>(tdK, tDS + (uint32_t)ks * 8u + (ks >= 4 ? 32u : 0u), mQ + mnmajor_step(ks), idK,
+              mma_ts_t<kW>(tdK, tDS + packed_col(ks), mQ + mnmajor_step(ks), idK,
                            (it > 0 || ks > 0) ? 1u : 0u);
             }
           }
@@ -412,12 +440,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mma_commit_t<kW>(bar(L::bDrain));
       drain_wait(bar(L::bDrain), 0);
     }
-  } else if (warp < 8) {
+  } else if (warp < W::kDrainWarp0) {
     // ------------------------------------------------------------ P and dS (thread = key row)
-    // warpgroup cw handles query columns 64 cw .. 64 cw + 63 of each tile
-    regs_inc<kComputeRegs>();
+    // warpgroup cw handles query columns kC cw .. kC cw + kC - 1 of each tile
+    regs_inc<W::kComputeRegs>();
+    constexpr int kC = W::kCols;
     const int cw = warp >> 2;
-    const int cb = 64 * cw;
+    const int cb = kC * cw;
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
@@ -449,55 +478,23 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const bool live = i < p.nT;
       for (int it = 0; i < p.nT; ++it, ++g, i = next_live(w, i + 1)) {
         const bool partial = tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kPartial;
-        const int s = g % L::kStages;
-        if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 120))) break;
-        if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 121))) break;
-        tc_fence_after();
-        if (p.chk.rec != nullptr && tid == 0) record_tile(p.chk.rec, w.bh, i, w.kj, p.nT, partial);   // as computed
-        const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
-        const float* dlt = lse2 + kTile;
-        float x[64];
-        {
-          uint32_t u0[32], u1[32];
-          tmem_ld32(tS + lane_off + (uint32_t)cb, u0);
-          tmem_ld32(tS + lane_off + (uint32_t)cb + 32u, u1);
-          tmem_ld_wait(u0);
-          tmem_ld_wait(u1);
+        // dropout: keep bits of this warpgroup's kC query columns, made before
+        // the waits below so that the generator runs while the tensor pipe
+        // computes S^T. One generator call (counter (query / 4, key / 4, bh,
+        // 0)) covers 4 queries, byte key mod 4 of each of its 4 words. The
+        // four key rows of a lane quad share their calls: each lane makes the
+        // call of one 4-query block, turns its 16 bytes into 16 keep bits (bit
+        // 4 j + k: query j, key k of the block) and the quad passes the masks
+        // around (one call per 16 queries and row instead of four)
+        uint32_t keep[kC / 32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            x[c] = __uint_as_float(u0[c]);
-            x[32 + c] = __uint_as_float(u1[c]);
-          }
-        }
-        // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = reinterpret_cast<const float4*>(lse2)[c4];   // one broadcast load per 4 queries
-          x[4 * c4] = ex2(fmaf(x[4 * c4], sl2, -l.x));
-          x[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], sl2, -l.y));
-          x[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], sl2, -l.z));
-          x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
-        }
-        if (partial) {
-          const int q0 = kTile * i + cb;
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
-        }
-        // dropout: keep bits of this warpgroup's 64 query columns; one generator
-        // call (counter (query / 4, key / 4, bh, 0)) covers 4 queries, byte
-        // key mod 4 of each of its 4 words. The four key rows of a lane quad
-        // share their calls: each lane makes the call of one 4-query block,
-        // turns its 16 bytes into 16 keep bits (bit 4 j + k: query j, key k of
-        // the block) and the quad passes the masks around (4 calls per row and
-        // tile instead of 16)
-        uint32_t keep[2] = {0u, 0u};
+        for (int q = 0; q < kC / 32; ++q) keep[q] = 0u;
         if constexpr (DROP) {
           const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
           const uint32_t s4 = (uint32_t)lane & 3u;   // = key row mod 4
           const uint32_t t4 = p.drop.t * 0x01010101u;
 #pragma unroll
-          for (int m4 = 0; m4 < 4; ++m4) {
+          for (int m4 = 0; m4 < kC / 16; ++m4) {
             const uint4 v = philox4x32_10(qb0 + 4u * (uint32_t)m4 + s4, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
                                           p.drop.seed_lo, p.drop.seed_hi);
             const uint32_t m16 = bytes_ge_nibble(v.x, t4) | (bytes_ge_nibble(v.y, t4) << 4) |
@@ -511,15 +508,54 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
               keep[m >> 3] |= bits << (4 * (m & 7));
             }
           }
+          // the bits are complete here: the compiler may not move the generator
+          // past the waits
+#pragma unroll
+          for (int q = 0; q < kC / 32; ++q) asm volatile("" : "+r"(keep[q]));
+        }
+        const int s = g % L::kStages;
+        if (!(ok = mbar_wait_warp(bar(L::bQFull + s), (uint32_t)(g / L::kStages) & 1u, ctl, 120))) break;
+        if (!(ok = mbar_wait_warp(bar(L::bSFull), (uint32_t)g & 1u, ctl, 121))) break;
+        tc_fence_after();
+        if (p.chk.rec != nullptr && tid == 0) record_tile(p.chk.rec, w.bh, i, w.kj, p.nT, partial);   // as computed
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kRow + s * 1024) + cb;
+        const float* dlt = lse2 + kTile;
+        float x[kC];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tS + lane_off + (uint32_t)cb, u0);
+          if constexpr (kC == 64) tmem_ld32(tS + lane_off + (uint32_t)cb + 32u, u1);
+          tmem_ld_wait(u0);
+          if constexpr (kC == 64) tmem_ld_wait(u1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(u0[c]);
+            if constexpr (kC == 64) x[32 + c] = __uint_as_float(u1[c]);
+          }
+        }
+        // P^T row: p[c] = exp2(s * scale * log2e - LSE2[query c])
+#pragma unroll
+        for (int c4 = 0; c4 < kC / 4; ++c4) {
+          const float4 l = reinterpret_cast<const float4*>(lse2)[c4];   // one broadcast load per 4 queries
+          x[4 * c4] = ex2(fmaf(x[4 * c4], sl2, -l.x));
+          x[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], sl2, -l.y));
+          x[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], sl2, -l.z));
+          x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
+        }
+        if (partial) {
+          const int q0 = kTile * i + cb;
+#pragma unroll
+          for (int c = 0; c < kC; ++c)
+            if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
         }
         auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
         // the dV operand is the dropped P (P * Z * keep_scale), packed two
         // queries per TMEM column into the first half of this warpgroup's own
         // S columns (the other warpgroup may still be reading its half)
         {
-          uint32_t pk[32];
+          uint32_t pk[kC / 2];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < kC / 2; ++c) {
             const int c0 = 2 * c;
             if constexpr (DROP)
               pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
@@ -527,7 +563,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             else
               pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
           }
-          tmem_st32(tS + lane_off + (uint32_t)cb, pk);
+          if constexpr (kC == 64) tmem_st32(tS + lane_off + (uint32_t)cb, pk);
+          else tmem_st16(tS + lane_off + (uint32_t)cb, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -539,7 +576,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (g > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(g - 1) & 1u, ctl, 123))) break;
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < kC / 32; ++cc) {
           uint32_t u[32];
           tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, u);
           tmem_ld_wait(u);
@@ -579,9 +616,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mbar_arrive_warp(bar(L::bdSFull));
       }
 
-      // epilogue: warpgroup 0 stores dV, warpgroup 1 scale * dK, for every key
-      // row of the tile (zeros when no query tile was live), staged in the
-      // item's V or K buffer once every MMA has read it, and stored by TMA
+      // epilogue: the first half of the warpgroups store dV, the second half
+      // scale * dK (each its share of the columns), for every key row of the
+      // tile (zeros when no query tile was live), staged in the item's V or K
+      // buffer once every MMA has read it, and stored by TMA
       ok = group_all(gbar, 128, ok);
       if (!ok) break;
       release_kv();   // the buffer of an earlier item without live query tiles
@@ -592,12 +630,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (!ok) break;
       nf += live ? 1 : 0;
       tc_fence_after();
-      const uint32_t tacc = (cw == 0 ? tdV : tdK) + lane_off;
-      const float mul = (cw == 0) ? 1.f : scale;
-      const int stage_off = (cw == 0 ? L::kV : L::kK) + kb * L::kKVBytes;
+      constexpr int kAccGroups = W::kGroups / 2;   // warpgroups per accumulator
+      constexpr int kAccCols = D / kAccGroups;       // columns each stores
+      const bool is_v = cw < kAccGroups;
+      const int col0 = kAccCols * (cw % kAccGroups);
+      const uint32_t tacc = (is_v ? tdV : tdK) + lane_off + (uint32_t)col0;
+      const float mul = is_v ? 1.f : scale;
+      const int stage_off = (is_v ? L::kV : L::kK) + kb * L::kKVBytes;
       uint8_t* stage = smem + stage_off;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < kAccCols / 32; ++cc) {
         uint32_t u[32];
         if (live) {
           tmem_ld32(tacc + 32u * cc, u);
@@ -612,7 +654,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           pk[c] = pack2<F16>(__uint_as_float(u[2 * c]) * mul, __uint_as_float(u[2 * c + 1]) * mul);
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
-          uint8_t* dst = stage + swz_off(r, 32 * cc + 8 * k4);
+          uint8_t* dst = stage + swz_off(r, col0 + 32 * cc + 8 * k4);
           *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
         }
       }
@@ -620,8 +662,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       fence_proxy_async_smem();
       named_bar_sync(gbar, 128);
       if (r == 0) {
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_store_3d(cw == 0 ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
+        for (int h = col0 / 64; h < (col0 + kAccCols) / 64; ++h)
+          tma_store_3d(is_v ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
         bulk_commit_group();
       }
       pending = kb;
@@ -629,7 +671,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (L::kKV == 1) release_kv();
     }
     if (r == 0) bulk_wait_group_read_all();   // the stores have read the staging; the grid's end makes them visible
-  } else if (warp < 12) {
+  } else if (warp < W::kProducerWarp) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
     // TMEM -> fp32 rows staged in this iteration's dO ring slot (dead once dQ
     // has completed) in two rounds of 32-column boxes, 128-byte swizzled ->
@@ -642,10 +684,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     //            meeting at named barriers; after each wait that one of them
     //            may fail they agree with group_all, so that they always take
     //            the same branch and none waits at a barrier another has left.
-    regs_dec<kDrainRegs>();
+    regs_dec<W::kDrainRegs>();
+    constexpr uint32_t kDrainBar = 1u + W::kGroups;   // named barrier of the drain warps (d = 64)
     constexpr int kBoxesPerRound = L::kTileBytes / 16384;    // 1 (d = 64) or 2 (d = 128)
     constexpr int kRounds = D / 32 / kBoxesPerRound;
-    const int r = tid - 256;
+    const int r = tid - 32 * W::kDrainWarp0;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t sw = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
     const uint32_t wrow = L::kGroupDrain ? 0u : 4096u * (uint32_t)(warp & 3);   // this warp's rows in a box
@@ -653,13 +696,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     int g = 0;
     for (int k = 0; ok; ++k) {
       const Item w = take_item(k, true, ok);
-      if constexpr (L::kGroupDrain) ok = group_all(3, 128, ok);
+      if constexpr (L::kGroupDrain) ok = group_all(kDrainBar, 128, ok);
       if (!ok || w.kj < 0) break;
       for (int i = next_live(w, 0); i < p.nT; ++g, i = next_live(w, i + 1)) {
         const int s = g % L::kStages;
         const uint32_t stage = (uint32_t)(L::kdO + s * L::kTileBytes);
         ok = mbar_wait_warp(bar(L::bdQFull), (uint32_t)g & 1u, ctl, 130);
-        if constexpr (L::kGroupDrain) ok = group_all(3, 128, ok);
+        if constexpr (L::kGroupDrain) ok = group_all(kDrainBar, 128, ok);
         if (!ok) break;
         tc_fence_after();
         uint32_t u[kBoxesPerRound][32];
@@ -676,7 +719,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (round > 0) {              // the previous round has been read out of the slot
             if constexpr (L::kGroupDrain) {
               if (r == 0) bulk_wait_group_read_all();
-              named_bar_sync(3, 128);
+              named_bar_sync(kDrainBar, 128);
             } else {
               if (lane == 0) bulk_wait_group_read_all();
               __syncwarp();
@@ -692,7 +735,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
           fence_proxy_async_smem();
           if constexpr (L::kGroupDrain)
-            named_bar_sync(3, 128);
+            named_bar_sync(kDrainBar, 128);
           else
             __syncwarp();
           if (L::kGroupDrain ? r == 0 : lane == 0) {
@@ -723,7 +766,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == W::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -828,7 +871,7 @@ cudaError_t launch_bwd_main_d(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.nT * p.B * p.H;
   const dim3 grid((unsigned)(items < sms ? items : sms));
-  return launch_pdl(true, fa_bwd_main_kernel<D, F16, DROP>, grid, dim3(kBwdThreads), L::kSmemBytes, s, tq, tk, tv, tdo,
+  return launch_pdl(true, fa_bwd_main_kernel<D, F16, DROP>, grid, dim3(BwdWarps<D, DROP>::kThreads), L::kSmemBytes, s, tq, tk, tv, tdo,
                     tdk, tdv, tdq, q, scale);
 }
 

@@ -497,6 +497,38 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t ent = list[e];
         if (!entry_live(ent, t)) continue;
+        // dropout: keep bits of this row for the entry's 128 keys (bit b of
+        // keep[q]: key 32 q + b), made before S is awaited, so that the
+        // generator runs while the tensor pipe computes S. Keep bytes of keys
+        // 4m .. 4m + 3 of a row come from one generator call, counter (row / 4,
+        // key / 4, bh, 0), word row mod 4, kept iff the byte >= t. The four rows
+        // of a lane quad share their calls: for every 16 keys each lane makes
+        // the call of one 4-key block, turns its four words into 16 bits (bit
+        // 4 j + k: row j of the quad, key k of the block) and takes from each
+        // lane of the quad the nibble of its own row
+        uint32_t keep[4] = {0u, 0u, 0u, 0u};
+        if constexpr (DROP) {
+          const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
+          const uint32_t s4 = (uint32_t)lane & 3u;   // = row mod 4
+          const uint32_t t4 = p.drop.t * 0x01010101u;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {   // keys 16 m .. 16 m + 15
+            const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 4u * (uint32_t)m + s4, (uint32_t)bh, 0u,
+                                          p.drop.seed_lo, p.drop.seed_hi);
+            const uint32_t m16 = bytes_ge_nibble(v.x, t4) | (bytes_ge_nibble(v.y, t4) << 4) |
+                                 (bytes_ge_nibble(v.z, t4) << 8) | (bytes_ge_nibble(v.w, t4) << 12);
+            uint32_t bits = 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {   // key block 4 m + u
+              const uint32_t mu = __shfl_sync(0xFFFFFFFFu, m16, (lane & ~3) | u);
+              bits |= ((mu >> (4u * s4)) & 0xFu) << (4 * u);
+            }
+            keep[m >> 1] |= bits << (16 * (m & 1));
+          }
+          // the bits are complete here: the compiler may not move the generator
+          // past the wait into the exponential loop
+          asm volatile("" : "+r"(keep[0]), "+r"(keep[1]), "+r"(keep[2]), "+r"(keep[3]));
+        }
         if (!mbar_wait_warp(bar(L::bSFull + t), nS & 1u, ctl, 10 + t)) { ok = false; break; }
         tc_fence_after();
         if (p.chk.rec != nullptr && r == 0) {   // the tile as this kernel computes it
@@ -592,14 +624,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           const float2 sl2x2 = make_float2(sl2, sl2);
           const float2 nref2 = make_float2(-ref, -ref);
           float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          // dropout: keep bytes of keys 4m .. 4m + 3 of this row come from one
-          // generator call, counter (row / 4, key / 4, bh, 0), word row mod 4. The
-          // four rows of a lane quad share their calls: for every 16 keys each
-          // lane makes the call of one 4-key block and a transpose across the
-          // quad hands every row its word of all four (one call per 16 keys and
-          // row instead of four)
-          const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
-          uint32_t kw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t pk[32];
@@ -610,19 +634,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               const float p1 = ex2(a.y);
               sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
               if constexpr (DROP) {
-                if ((i & 7) == 0) {
-                  const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 16u * hh + (uint32_t)(i >> 1) + ((uint32_t)lane & 3u),
-                                                (uint32_t)bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
-                  kw[0] = v.x;
-                  kw[1] = v.y;
-                  kw[2] = v.z;
-                  kw[3] = v.w;
-                  quad_transpose(kw, (uint32_t)lane & 3u);   // kw[j]: word (row mod 4) of key block (i / 2) + j
-                }
-                const uint32_t rw = kw[(i >> 1) & 3];
-                const uint32_t sh = 16u * (uint32_t)(i & 1);
-                const float d0 = ((rw >> sh) & 0xFFu) >= p.drop.t ? p0 * p.drop.keep_scale : 0.f;
-                const float d1 = ((rw >> (sh + 8u)) & 0xFFu) >= p.drop.t ? p1 * p.drop.keep_scale : 0.f;
+                const uint32_t kq = keep[2 * hh + (i >> 4)] >> (2 * (i & 15));   // keys 64 hh + 2 i, + 1
+                const float d0 = (kq & 1u) ? p0 * p.drop.keep_scale : 0.f;
+                const float d1 = (kq & 2u) ? p1 * p.drop.keep_scale : 0.f;
                 pk[i] = pack2<F16>(d0, d1);
               } else {
                 pk[i] = pack2<F16>(p0, p1);
