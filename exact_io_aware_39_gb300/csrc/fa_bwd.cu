@@ -480,34 +480,38 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const bool partial = tile_state(i, w.kj, w.kvl, p.nT, p.causal, p.block_mask) == kPartial;
         // dropout: keep bits of this warpgroup's kC query columns, made before
         // the waits below so that the generator runs while the tensor pipe
-        // computes S^T. One generator call (counter (query / 4, key / 4, bh,
-        // 0)) covers 4 queries, byte key mod 4 of each of its 4 words. The
-        // four key rows of a lane quad share their calls: each lane makes the
-        // call of one 4-query block, turns its 16 bytes into 16 keep bits (bit
-        // 4 j + k: query j, key k of the block) and the quad passes the masks
-        // around (one call per 16 queries and row instead of four)
+        // computes S^T. One generator call (counter (query block, key block,
+        // bh, 0)) covers 4 queries (word d: query d of the block) and 4 keys
+        // (byte k: key k); a query is kept iff its byte is >= t. The four key
+        // rows of a lane quad share their calls: lane s makes the calls of
+        // query blocks 4 m4 + s and files the flags of call m4, word d in bit
+        // 4 (m4 mod 2) + d of byte k of w2[m4 / 2]; byte k of w2[0] and w2[1]
+        // goes to key row k of the quad, by a 4 x 4 transpose across the quad.
+        // Query column c = 16 m4 + 4 j + d is then bit 4 m4 + d of word j,
+        // packed kPer words of kBits bits to a register (kept() below).
+        constexpr int kPer = 128 / kC, kBits = kC / 4;
         uint32_t keep[kC / 32];
 #pragma unroll
         for (int q = 0; q < kC / 32; ++q) keep[q] = 0u;
         if constexpr (DROP) {
           const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
           const uint32_t s4 = (uint32_t)lane & 3u;   // = key row mod 4
-          const uint32_t t4 = p.drop.t * 0x01010101u;
+          const uint32_t c4 = (256u - p.drop.t) * 0x01010101u;
+          uint32_t w2[2] = {0u, 0u};
 #pragma unroll
           for (int m4 = 0; m4 < kC / 16; ++m4) {
             const uint4 v = philox4x32_10(qb0 + 4u * (uint32_t)m4 + s4, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
                                           p.drop.seed_lo, p.drop.seed_hi);
-            const uint32_t m16 = bytes_ge_nibble(v.x, t4) | (bytes_ge_nibble(v.y, t4) << 4) |
-                                 (bytes_ge_nibble(v.z, t4) << 8) | (bytes_ge_nibble(v.w, t4) << 12);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t mu = __shfl_sync(0xFFFFFFFFu, m16, (lane & ~3) | u);   // query block 4 m4 + u
-              const uint32_t b = (mu >> s4) & 0x1111u;
-              const uint32_t bits = (b | (b >> 3) | (b >> 6) | (b >> 9)) & 0xFu;   // queries 0..3 of the block
-              const int m = 4 * m4 + u;
-              keep[m >> 3] |= bits << (4 * (m & 7));
-            }
+            const int sh = 4 * (m4 & 1);
+            w2[m4 >> 1] |= (bytes_ge_flags(v.x, c4) >> (7 - sh)) | (bytes_ge_flags(v.y, c4) >> (6 - sh)) |
+                           (bytes_ge_flags(v.z, c4) >> (5 - sh)) | (bytes_ge_flags(v.w, c4) >> (4 - sh));
           }
+          uint32_t x4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) x4[k] = ((w2[0] >> (8 * k)) & 0xFFu) | (((w2[1] >> (8 * k)) & 0xFFu) << 8);
+          quad_transpose(x4, s4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) keep[j / kPer] |= x4[j] << (kBits * (j % kPer));
           // the bits are complete here: the compiler may not move the generator
           // past the waits
 #pragma unroll
@@ -548,7 +552,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           for (int c = 0; c < kC; ++c)
             if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
         }
-        auto kept = [&](int c) -> bool { return (keep[c >> 5] >> (c & 31)) & 1u; };
+        auto kept = [&](int c) -> bool {
+          const int j = (c >> 2) & 3;
+          return (keep[j / kPer] >> (kBits * (j % kPer) + 4 * (c >> 4) + (c & 3))) & 1u;
+        };
         // the dV operand is the dropped P (P * Z * keep_scale), packed two
         // queries per TMEM column into the first half of this warpgroup's own
         // S columns (the other warpgroup may still be reading its half)

@@ -497,34 +497,31 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t ent = list[e];
         if (!entry_live(ent, t)) continue;
-        // dropout: keep bits of this row for the entry's 128 keys (bit b of
-        // keep[q]: key 32 q + b), made before S is awaited, so that the
-        // generator runs while the tensor pipe computes S. Keep bytes of keys
-        // 4m .. 4m + 3 of a row come from one generator call, counter (row / 4,
-        // key / 4, bh, 0), word row mod 4, kept iff the byte >= t. The four rows
-        // of a lane quad share their calls: for every 16 keys each lane makes
-        // the call of one 4-key block, turns its four words into 16 bits (bit
-        // 4 j + k: row j of the quad, key k of the block) and takes from each
-        // lane of the quad the nibble of its own row
+        // dropout: keep bits of this row for the entry's 128 keys, made before S
+        // is awaited, so that the generator runs while the tensor pipe computes
+        // S. Keep bytes of keys 4b .. 4b + 3 of a row come from one generator
+        // call, counter (row / 4, key block b, bh, 0), word row mod 4; a key is
+        // kept iff its byte is >= t. The four rows of a lane quad share their
+        // calls: for keys 16m .. 16m + 15 lane s of the quad makes the call of
+        // key block 4m + s and files the flags of word d (row d of the quad) in
+        // bits 8k + m of word d (k: key of the block); a 4 x 4 transpose across
+        // the quad then hands every row its four words. keep[s] bit 8k + m:
+        // key 16m + 4s + k of the entry.
         uint32_t keep[4] = {0u, 0u, 0u, 0u};
         if constexpr (DROP) {
           const uint32_t kb0 = 32u * (uint32_t)entry_j(ent);
           const uint32_t s4 = (uint32_t)lane & 3u;   // = row mod 4
-          const uint32_t t4 = p.drop.t * 0x01010101u;
+          const uint32_t c4 = (256u - p.drop.t) * 0x01010101u;
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {   // keys 16 m .. 16 m + 15
+          for (int m = 0; m < 8; ++m) {
             const uint4 v = philox4x32_10((uint32_t)row >> 2, kb0 + 4u * (uint32_t)m + s4, (uint32_t)bh, 0u,
                                           p.drop.seed_lo, p.drop.seed_hi);
-            const uint32_t m16 = bytes_ge_nibble(v.x, t4) | (bytes_ge_nibble(v.y, t4) << 4) |
-                                 (bytes_ge_nibble(v.z, t4) << 8) | (bytes_ge_nibble(v.w, t4) << 12);
-            uint32_t bits = 0u;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {   // key block 4 m + u
-              const uint32_t mu = __shfl_sync(0xFFFFFFFFu, m16, (lane & ~3) | u);
-              bits |= ((mu >> (4u * s4)) & 0xFu) << (4 * u);
-            }
-            keep[m >> 1] |= bits << (16 * (m & 1));
+            keep[0] |= bytes_ge_flags(v.x, c4) >> (7 - m);
+            keep[1] |= bytes_ge_flags(v.y, c4) >> (7 - m);
+            keep[2] |= bytes_ge_flags(v.z, c4) >> (7 - m);
+            keep[3] |= bytes_ge_flags(v.w, c4) >> (7 - m);
           }
+          quad_transpose(keep, s4);
           // the bits are complete here: the compiler may not move the generator
           // past the wait into the exponential loop
           asm volatile("" : "+r"(keep[0]), "+r"(keep[1]), "+r"(keep[2]), "+r"(keep[3]));
@@ -634,9 +631,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               const float p1 = ex2(a.y);
               sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
               if constexpr (DROP) {
-                const uint32_t kq = keep[2 * hh + (i >> 4)] >> (2 * (i & 15));   // keys 64 hh + 2 i, + 1
-                const float d0 = (kq & 1u) ? p0 * p.drop.keep_scale : 0.f;
-                const float d1 = (kq & 2u) ? p1 * p.drop.keep_scale : 0.f;
+                // keys 64 hh + 2 i and + 1: m = 4 hh + i / 8, s = (i / 2) mod 4, k = 2 (i mod 2)
+                const uint32_t kw = keep[(i >> 1) & 3];
+                const int m = 4 * hh + (i >> 3), k = 2 * (i & 1);
+                const float d0 = ((kw >> (8 * k + m)) & 1u) ? p0 * p.drop.keep_scale : 0.f;
+                const float d1 = ((kw >> (8 * k + 8 + m)) & 1u) ? p1 * p.drop.keep_scale : 0.f;
                 pk[i] = pack2<F16>(d0, d1);
               } else {
                 pk[i] = pack2<F16>(p0, p1);

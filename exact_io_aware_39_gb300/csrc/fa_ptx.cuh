@@ -592,19 +592,15 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&x)[4], uint32_t s) {
   if (h2) { x[0] = v0; x[1] = v1; } else { x[2] = v0; x[3] = v1; }
 }
 
-// Bit k (k = 0..3) set when byte k of w is >= the byte of t4 (t4 = t repeated
-// in all four bytes), unsigned. Bytewise a >= b is "a - b does not borrow":
-// with the top bits set aside, (a | 0x80..) - (b & 0x7F..) leaves in bit 7 of
-// each byte whether the low 7 bits of a are >= those of b; the top bits then
-// decide where a and b differ there.
-__device__ __forceinline__ uint32_t bytes_ge_nibble(uint32_t w, uint32_t t4) {
-  const uint32_t d = (w | 0x80808080u) - (t4 & 0x7F7F7F7Fu);
-  const uint32_t g = ((w & ~t4) | (~(w ^ t4) & d)) & 0x80808080u;
-  return ((g >> 7) | (g >> 14) | (g >> 21) | (g >> 28)) & 0xFu;
-}
-
-__device__ __forceinline__ uint32_t uint4_word(const uint4& v, uint32_t i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+// Keep flags of the four bytes of w, in bit 7 of each byte: set where the byte
+// is >= t (1 <= t <= 255), unsigned, given c4 = (256 - t) repeated in all four
+// bytes. b >= t exactly when b + (256 - t) carries out of the byte. Added
+// without the top bits, the bytes cannot carry into one another, and bit 7
+// of each sum byte is the carry out of the low seven bits; the carry out of
+// the byte is then the majority of that carry and the two top bits.
+__device__ __forceinline__ uint32_t bytes_ge_flags(uint32_t w, uint32_t c4) {
+  const uint32_t s = (w & 0x7F7F7F7Fu) + (c4 & 0x7F7F7F7Fu);
+  return ((w & c4) | ((w | c4) & s)) & 0x80808080u;
 }
 
 __device__ __forceinline__ void red_add_v4(float* gptr, float a, float b, float c, float d) {
