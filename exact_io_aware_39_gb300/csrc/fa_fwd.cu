@@ -630,15 +630,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               const float p0 = ex2(a.x);
               const float p1 = ex2(a.y);
               sum4[i & 3] = __fadd2_rn(sum4[i & 3], make_float2(p0, p1));   // statistics use the undropped P
+              pk[i] = pack2<F16>(p0, p1);
               if constexpr (DROP) {
-                // keys 64 hh + 2 i and + 1: m = 4 hh + i / 8, s = (i / 2) mod 4, k = 2 (i mod 2)
-                const uint32_t kw = keep[(i >> 1) & 3];
+                // keys 64 hh + 2 i and + 1 are bits 8k + m and 8k + 8 + m of
+                // keep[(i / 2) mod 4] (m = 4 hh + i / 8, k = 2 (i mod 2)): shifted
+                // to bit 7 of bytes k and k + 1, they become the masks of the
+                // two 16-bit halves by sign replication. The keep scale is
+                // applied to O in the epilogue (the same factor for every kept term).
                 const int m = 4 * hh + (i >> 3), k = 2 * (i & 1);
-                const float d0 = ((kw >> (8 * k + m)) & 1u) ? p0 * p.drop.keep_scale : 0.f;
-                const float d1 = ((kw >> (8 * k + 8 + m)) & 1u) ? p1 * p.drop.keep_scale : 0.f;
-                pk[i] = pack2<F16>(d0, d1);
-              } else {
-                pk[i] = pack2<F16>(p0, p1);
+                const uint32_t kw = keep[(i >> 1) & 3] << (7 - m);
+                pk[i] &= prmt(kw, 0u, (uint32_t)((8 + k) * 0x11 + (9 + k) * 0x1100));
               }
             }
             tmem_st32(tP + 32u * hh, pk);
@@ -668,7 +669,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         if (!ok) drain_wait(bar(L::bQFull), kq & 1u);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
         tc_fence_after();
         uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
-        const float inv_l = (n > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (n > 0 && l > 0.f) ? (DROP ? p.drop.keep_scale : 1.f) / l : 0.f;
         const bool have_o = ok && n > 0;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {

@@ -592,6 +592,15 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&x)[4], uint32_t s) {
   if (h2) { x[0] = v0; x[1] = v1; } else { x[2] = v0; x[3] = v1; }
 }
 
+// Byte permute (PTX prmt.b32, default mode): byte n of the result is chosen
+// by nibble n of sel from the eight bytes of {b, a} (0-3: a, 4-7: b); when the
+// nibble's top bit is set the chosen byte's bit 7 is copied to all 8 bits.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 // Keep flags of the four bytes of w, in bit 7 of each byte: set where the byte
 // is >= t (1 <= t <= 255), unsigned, given c4 = (256 - t) repeated in all four
 // bytes. b >= t exactly when b + (256 - t) carries out of the byte. Added
