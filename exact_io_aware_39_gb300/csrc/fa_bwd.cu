@@ -485,11 +485,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         // (byte k: key k); a query is kept iff its byte is >= t. The four key
         // rows of a lane quad share their calls: lane s makes the calls of
         // query blocks 4 m4 + s and files the flags of call m4, word d in bit
-        // 4 (m4 mod 2) + d of byte k of w2[m4 / 2]; byte k of w2[0] and w2[1]
-        // goes to key row k of the quad, by a 4 x 4 transpose across the quad.
-        // Query column c = 16 m4 + 4 j + d is then bit 4 m4 + d of word j,
-        // packed kPer words of kBits bits to a register (kept() below).
-        constexpr int kPer = 128 / kC, kBits = kC / 4;
+        // 2 m4 + d / 2 of byte k of ev (d even) or od (d odd); bytes k of ev
+        // and od go to key row k of the quad, by a 4 x 4 transpose across the
+        // quad. Query column c = 16 m4 + 4 j + d is then bit
+        // kbase(j) + 8 (d mod 2) + 2 m4 + d / 2 of keep[kword(j)]: the two
+        // queries of a pair (d, d + 1) sit 8 bits apart (see pair_mask).
+        auto kword = [](int j) { return kC == 64 ? (j >> 1) : 0; };
+        auto kbase = [](int j) { return kC == 64 ? 16 * (j & 1) : 16 * (j >> 1) + 4 * (j & 1); };
         uint32_t keep[kC / 32];
 #pragma unroll
         for (int q = 0; q < kC / 32; ++q) keep[q] = 0u;
@@ -497,21 +499,20 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const uint32_t qb0 = 32u * (uint32_t)i + (uint32_t)(cb >> 2);
           const uint32_t s4 = (uint32_t)lane & 3u;   // = key row mod 4
           const uint32_t c4 = (256u - p.drop.t) * 0x01010101u;
-          uint32_t w2[2] = {0u, 0u};
+          uint32_t ev = 0u, od = 0u;
 #pragma unroll
           for (int m4 = 0; m4 < kC / 16; ++m4) {
             const uint4 v = philox4x32_10(qb0 + 4u * (uint32_t)m4 + s4, (uint32_t)krow >> 2, (uint32_t)w.bh, 0u,
                                           p.drop.seed_lo, p.drop.seed_hi);
-            const int sh = 4 * (m4 & 1);
-            w2[m4 >> 1] |= (bytes_ge_flags(v.x, c4) >> (7 - sh)) | (bytes_ge_flags(v.y, c4) >> (6 - sh)) |
-                           (bytes_ge_flags(v.z, c4) >> (5 - sh)) | (bytes_ge_flags(v.w, c4) >> (4 - sh));
+            ev |= (bytes_ge_flags(v.x, c4) >> (7 - 2 * m4)) | (bytes_ge_flags(v.z, c4) >> (6 - 2 * m4));
+            od |= (bytes_ge_flags(v.y, c4) >> (7 - 2 * m4)) | (bytes_ge_flags(v.w, c4) >> (6 - 2 * m4));
           }
           uint32_t x4[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) x4[k] = ((w2[0] >> (8 * k)) & 0xFFu) | (((w2[1] >> (8 * k)) & 0xFFu) << 8);
+          for (int k = 0; k < 4; ++k) x4[k] = ((ev >> (8 * k)) & 0xFFu) | (((od >> (8 * k)) & 0xFFu) << 8);
           quad_transpose(x4, s4);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) keep[j / kPer] |= x4[j] << (kBits * (j % kPer));
+          for (int j = 0; j < 4; ++j) keep[kword(j)] |= x4[j] << (kC == 64 ? 16 * (j & 1) : 16 * (j >> 1) + 4 * (j & 1));
           // the bits are complete here: the compiler may not move the generator
           // past the waits
 #pragma unroll
@@ -553,22 +554,27 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
         }
         auto kept = [&](int c) -> bool {
-          const int j = (c >> 2) & 3;
-          return (keep[j / kPer] >> (kBits * (j % kPer) + 4 * (c >> 4) + (c & 3))) & 1u;
+          const int j = (c >> 2) & 3, d = c & 3;
+          return (keep[kword(j)] >> (kbase(j) + 8 * (d & 1) + 2 * (c >> 4) + (d >> 1))) & 1u;
         };
-        // the dV operand is the dropped P (P * Z * keep_scale), packed two
+        // masks of the two 16-bit halves of the packed pair of queries c0, c0 + 1
+        // (c0 even): their bits, shifted to bit 7 of two bytes, are replicated
+        // by prmt over the bytes of each half
+        auto pair_mask = [&](int c0) -> uint32_t {
+          const int j = (c0 >> 2) & 3, b0 = kbase(j) >> 3;
+          const int pos = (kbase(j) & 7) + 2 * (c0 >> 4) + ((c0 & 3) >> 1);
+          return prmt(keep[kword(j)] << (7 - pos), 0u, (uint32_t)((8 + b0) * 0x11 + (9 + b0) * 0x1100));
+        };
+        // the dV operand is the dropped P (P * Z; the keep scale, the same for
+        // every kept term, is applied to dV in the epilogue), packed two
         // queries per TMEM column into the first half of this warpgroup's own
         // S columns (the other warpgroup may still be reading its half)
         {
           uint32_t pk[kC / 2];
 #pragma unroll
           for (int c = 0; c < kC / 2; ++c) {
-            const int c0 = 2 * c;
-            if constexpr (DROP)
-              pk[c] = pack2<F16>(kept(c0) ? x[c0] * p.drop.keep_scale : 0.f,
-                                 kept(c0 + 1) ? x[c0 + 1] * p.drop.keep_scale : 0.f);
-            else
-              pk[c] = pack2<F16>(x[c0], x[c0 + 1]);
+            pk[c] = pack2<F16>(x[2 * c], x[2 * c + 1]);
+            if constexpr (DROP) pk[c] &= pair_mask(2 * c);
           }
           if constexpr (kC == 64) tmem_st32(tS + lane_off + (uint32_t)cb, pk);
           else tmem_st16(tS + lane_off + (uint32_t)cb, pk);
@@ -592,13 +598,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           for (int c = 0; c < 16; ++c) {
             const int c0 = 32 * cc + 2 * c;
             float g0 = __uint_as_float(u[2 * c]), g1 = __uint_as_float(u[2 * c + 1]);
-            if constexpr (DROP) {   // dP = (dO V^T) * Z * keep_scale
-              g0 = kept(c0) ? g0 * p.drop.keep_scale : 0.f;
-              g1 = kept(c0 + 1) ? g1 * p.drop.keep_scale : 0.f;
-            }
             const float2 dl = reinterpret_cast<const float2*>(dlt)[c0 >> 1];
-            const float d0 = x[c0] * (g0 - dl.x);
-            const float d1 = x[c0 + 1] * (g1 - dl.y);
+            float d0, d1;
+            if constexpr (DROP) {   // dP = (dO V^T) * Z * keep_scale
+              g0 = kept(c0) ? g0 : 0.f;
+              g1 = kept(c0 + 1) ? g1 : 0.f;
+              d0 = x[c0] * fmaf(g0, p.drop.keep_scale, -dl.x);
+              d1 = x[c0 + 1] * fmaf(g1, p.drop.keep_scale, -dl.y);
+            } else {
+              d0 = x[c0] * (g0 - dl.x);
+              d1 = x[c0 + 1] * (g1 - dl.y);
+            }
             pk[c] = pack2<F16>(d0, d1);
           }
           // dS^T also goes to TMEM (the A operand of dK), packed: at d = 128 into
@@ -642,7 +652,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const bool is_v = cw < kAccGroups;
       const int col0 = kAccCols * (cw % kAccGroups);
       const uint32_t tacc = (is_v ? tdV : tdK) + lane_off + (uint32_t)col0;
-      const float mul = is_v ? 1.f : scale;
+      const float mul = is_v ? (DROP ? p.drop.keep_scale : 1.f) : scale;
       const int stage_off = (is_v ? L::kV : L::kK) + kb * L::kKVBytes;
       uint8_t* stage = smem + stage_off;
 #pragma unroll
