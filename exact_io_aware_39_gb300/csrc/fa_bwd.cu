@@ -238,10 +238,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   constexpr bool kOwnDQ = (D == 64);
   constexpr bool kSplitDS = (D == 128) && W::kGroups == 2;   // dS^T handed to dK in two halves
   const uint32_t tQ = kOwnDQ ? tmem + 2u * D + 256u : tP;
-  // dS^T for dK: packed into the S columns next to P^T at d = 128 (S^T of the
-  // next tile is issued after dK), into the dP^T columns at d = 64 (S^T of
-  // the next tile is issued before dK)
-  const uint32_t tDS = kOwnDQ ? tP : tS + (uint32_t)(W::kCols / 2);
+  // S^T of the next tile right behind dV (before dK) at d = 64, and at d = 128
+  // with dropout, where the P/dS warps bound the kernel and the next P then
+  // overlaps dK and dQ (measured: +2 % there, -2.5 % at d = 128 without
+  // dropout, where the dQ drain then sits in front of the next dP^T)
+  constexpr bool kEarlyS = kOwnDQ || DROP;
+  // dS^T for dK: packed over the consumed dP^T columns when the next S^T is
+  // issued before dK (dQ, which reuses those columns at d = 128, is issued
+  // after dK, and the tensor pipe runs in issue order), else into the S
+  // columns next to P^T
+  const uint32_t tDS = kEarlyS ? tP : tS + (uint32_t)(W::kCols / 2);
   // TMEM column of K step ks (16 queries) of the packed P^T / dS^T: each
   // warpgroup packs its kCols queries into the first kCols / 2 of its own
   // kCols S (or dP^T) columns
@@ -399,11 +405,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             // P of each warpgroup's queries packed in the first half of its own S columns
             mma_ts_t<kW>(tdV, tS + packed_col(ks), mdO + mnmajor_step(ks), idV,
                    (it > 0 || ks > 0) ? 1u : 0u);
-          // next S^T of this item: at d = 64 right behind dV (the tensor pipe
+          // next S^T of this item: early, right behind dV (the tensor pipe
           // runs in issue order, so dV has read P first), so that P of the
-          // next tile is recomputed while dK, dQ and the next dP run; at
-          // d = 128 after dQ, which leaves the next Q load the longest window
-          if (kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
+          // next tile is recomputed while dK, dQ and the next dP run; else
+          // after dQ, which leaves the next Q load the longest window
+          if (kEarlyS && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
           // dK += dS^T Q ; dQ_i = dS K. dS^T is packed like P (packed_col) from
           // tDS on; with two warpgroups, at d = 128 each
           // warpgroup hands over its first 32 queries (K steps 0, 1 and 4, 5)
@@ -432,7 +438,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mma_ss_t<kW>(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
           mma_commit_t<kW>(bar(L::bdQFull));
           mma_commit_t<kW>(bar(L::bdSEmpty));      // dK and dQ have read dS
-          if (!kOwnDQ && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
+          if (!kEarlyS && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
           i = inext;
         }
         if (ok) mma_commit_t<kW>(bar(L::bFinal));   // dV and dK of the item are complete
@@ -611,9 +617,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             }
             pk[c] = pack2<F16>(d0, d1);
           }
-          // dS^T also goes to TMEM (the A operand of dK), packed: at d = 128 into
-          // the second half of this warpgroup's S columns, after its P; at d = 64
-          // over this warpgroup's dP columns, which it has already read
+          // dS^T also goes to TMEM (the A operand of dK), packed (tDS): over
+          // this warpgroup's dP columns, which it has already read, or into the
+          // second half of its S columns, after its P
           tmem_st16(tDS + lane_off + (uint32_t)cb + 16u * cc, pk);
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
