@@ -56,17 +56,17 @@ namespace {
 // Warp roles of the main kernel. kGroups P/dS warpgroups split each tile's
 // 128 query columns (kCols each), then one warpgroup drains dQ and one holds
 // the TMA producer, the MMA warp and two idle warps. Four groups of 32
-// queries only at d = 128 with dropout, where the keep bits (Philox rounds)
-// make the P/dS work the bound (measured: backward main +8 % there, -6 %
-// without dropout, where two groups with more registers each run ahead of
-// the tensor pipe by less). The registers after
+// queries with dropout, where the keep bits (generator rounds) make the P/dS
+// work the bound (measured on the backward main kernel: +8 % at d = 128,
+// +10 % at d = 64; without dropout -6 % at d = 128 and -5 % to +1 % at
+// d = 64, where two groups of more registers each do better). The registers after
 // reallocation add up to what the CTA is launched with (setmaxnreg.inc
 // draws on that, not on the SM): 2 groups, 512 threads launched at 128:
 // 2 x 128 x 160 + 128 x 96 + 128 x 96 = 512 x 128; 4 groups, 768 threads
 // launched at 80: 4 x 128 x 88 + 128 x 72 + 128 x 56 = 768 x 80.
 template <int D, bool DROP>
 struct BwdWarps {
-  static constexpr int kGroups = (D == 128 && DROP) ? 4 : 2;
+  static constexpr int kGroups = DROP ? 4 : 2;
   static constexpr int kCols = kTile / kGroups;
   static constexpr int kThreads = 128 * (kGroups + 2);
   static constexpr int kDrainWarp0 = 4 * kGroups;
@@ -474,10 +474,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     // epilogue; before it, and wherever one of them may have stopped (a wait
     // that ran out or saw the abort flag), they agree with group_all, so that
     // all of them take the same branch and none waits for one that has left.
-    const uint32_t gbar = 1u + (uint32_t)cw;
+    // Where two groups share a 64-column store box of dV or dK (d = 64 with
+    // four groups), all the groups meet and agree together instead.
+    constexpr int kAccGroups = W::kGroups / 2;   // warpgroups per accumulator
+    constexpr int kAccCols = D / kAccGroups;       // columns each stores
+    constexpr bool kJoint = kAccCols < 64;
+    const uint32_t gbar = kJoint ? 1u : 1u + (uint32_t)cw;
+    constexpr uint32_t kGThreads = kJoint ? 128u * W::kGroups : 128u;
     for (int k = 0; ok; ++k) {
       const Item w = take_item(k, true, ok);
-      ok = group_all(gbar, 128, ok);
+      ok = group_all(gbar, kGThreads, ok);
       if (!ok || w.kj < 0) break;
       const int krow = kTile * w.kj + r;
       int i = next_live(w, 0);
@@ -643,18 +649,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       // scale * dK (each its share of the columns), for every key row of the
       // tile (zeros when no query tile was live), staged in the item's V or K
       // buffer once every MMA has read it, and stored by TMA
-      ok = group_all(gbar, 128, ok);
+      ok = group_all(gbar, kGThreads, ok);
       if (!ok) break;
       release_kv();   // the buffer of an earlier item without live query tiles
       const int kb = k % L::kKV;
       ok = mbar_wait_warp(bar(L::bKV + kb), (uint32_t)(k / L::kKV) & 1u, ctl, 124);
       if (ok && live) ok = mbar_wait_warp(bar(L::bFinal), (uint32_t)nf & 1u, ctl, 125);
-      ok = group_all(gbar, 128, ok);
+      ok = group_all(gbar, kGThreads, ok);
       if (!ok) break;
       nf += live ? 1 : 0;
       tc_fence_after();
-      constexpr int kAccGroups = W::kGroups / 2;   // warpgroups per accumulator
-      constexpr int kAccCols = D / kAccGroups;       // columns each stores
       const bool is_v = cw < kAccGroups;
       const int col0 = kAccCols * (cw % kAccGroups);
       const uint32_t tacc = (is_v ? tdV : tdK) + lane_off + (uint32_t)col0;
@@ -683,9 +687,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      named_bar_sync(gbar, 128);
-      if (r == 0) {
-        for (int h = col0 / 64; h < (col0 + kAccCols) / 64; ++h)
+      named_bar_sync(gbar, kGThreads);
+      if (r == 0 && col0 % 64 == 0) {   // a shared box: its first group stores it
+        for (int h = col0 / 64; h < (col0 + (kJoint ? 64 : kAccCols)) / 64; ++h)
           tma_store_3d(is_v ? &tdv : &tdk, sbase + stage_off + h * 16384, 64 * h, kTile * w.kj, w.bh);
         bulk_commit_group();
       }
