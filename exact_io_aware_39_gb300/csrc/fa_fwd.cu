@@ -17,7 +17,8 @@
 //       warps 0-3  softmax / correction / epilogue of Q tile 0 (TMEM lanes 0-127)
 //       warps 4-7  the same for Q tile 1
 //       warp  8    builds each item's list of live key tiles; TMA producer of
-//                  Q and of the K ring; asks for the next item
+//                  Q and of the K ring; asks for the next item and, at d = 64
+//                  (two Q buffers), sets it up while the current one runs
 //       warp  9    TMEM allocator; runs the MMA schedule (one lane picked by
 //                  elect.sync issues each tcgen05.mma)
 //       warp 10    TMA producer of the V ring
@@ -59,21 +60,26 @@ struct FwdLayout {
   static constexpr int kHalves = D / 64;
   // separate K and V rings; the K ring is the deeper one, since the S MMAs
   // that read K come first
-  static constexpr int kStagesK = (D == 64) ? 6 : 3;
-  static constexpr int kStagesV = (D == 64) ? 5 : 2;
+  static constexpr int kStagesK = (D == 64) ? 5 : 3;
+  static constexpr int kStagesV = (D == 64) ? 4 : 2;
+  // Q buffers (each the two Q tiles of an item, and then the item's O
+  // staging) and key-tile lists: at d = 64 two, so that the next item's list
+  // is built and its Q and first K tiles are loaded while this item runs; at
+  // d = 128 the shared memory holds one
   // At d = 64, S_0, S_1 (128 columns each) and O_0, O_1 (64 each) leave 128
   // TMEM columns, which give each Q tile's P columns of their own: S_t is then
   // free as soon as its softmax group has read it into registers, and the
   // next S_t is computed while that group works on this one. At d = 128 the
   // four regions fill TMEM and P is packed over S in place.
   static constexpr bool kOwnP = (D == 64);
+  static constexpr int kQBuf = (D == 64) ? 2 : 1;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kK = kQ + kQBuf * 2 * kTileBytes;
   static constexpr int kV = kK + kStagesK * kTileBytes;
   static constexpr int kBar = kV + kStagesV * kTileBytes;   // 8-byte mbarriers
   // barrier slots
-  static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;
+  static constexpr int bQFull = 0;                    // [kQBuf]
+  static constexpr int bKFull = bQFull + kQBuf;
   static constexpr int bKEmpty = bKFull + kStagesK;
   static constexpr int bVFull = bKEmpty + kStagesK;
   static constexpr int bVEmpty = bVFull + kStagesV;
@@ -85,12 +91,13 @@ struct FwdLayout {
   static constexpr int bClc = bPVDone + 2;            // the next item's cancellation answer has arrived
   static constexpr int bDrain = bClc + 1;
   static constexpr int kNumBars = bDrain + 1;
-  // tmem slot, abort flag, list length, wait limit, last list entry live for
-  // Q tile 0 and 1, next item, -
+  // 32-bit words: tmem slot, abort flag, -, wait limit, -, -, next item, -;
+  // then per buffer b at 8 + 4 b: list length, last list entry live for Q
+  // tile 0 and for Q tile 1, -
   static constexpr int kMisc = kBar + 8 * kNumBars;
-  static constexpr int kClc = (kMisc + 32 + 15) & ~15;   // 16-byte answer of a launch cancellation
-  static constexpr int kList = kClc + 16;                // uint16 entries
-  static constexpr int kSmemBytes = kList + 2 * kListMax;
+  static constexpr int kClc = (kMisc + 4 * (8 + 4 * kQBuf) + 15) & ~15;   // 16-byte answer of a launch cancellation
+  static constexpr int kList = kClc + 16;                // uint16 entries, kListMax per buffer
+  static constexpr int kSmemBytes = kList + kQBuf * 2 * kListMax;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -182,33 +189,33 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   };
   if (warp == 8) {
     regs_dec<kOtherRegs>();
-    for (;; ++kq) {
+    uint32_t nq[2] = {0u, 0u};   // Q loads issued into each buffer (lane 0)
+    // Sets item `it` up in buffer qb: its Q tiles are loaded, the union list
+    // of the key tiles live for either Q tile is built (ascending j) with its
+    // length and the last entry live for each tile, and the K tiles of the
+    // first ring's worth of entries are loaded (K ring entries base, base + 1,
+    // ...), so that their loads overlap the rest of the set-up. Returns (on
+    // lane 0) the K loads issued.
+    auto setup = [&](int it, int qb, int base) -> int {
       int bh = 0;
-      const int c = nC - 1 - split_grouped(item, p.group, nC, BH, &bh);
-      const int b = bh / p.H;
+      const int c = nC - 1 - split_grouped(it, p.group, nC, BH, &bh);
       const int qi0 = 2 * c;
       const bool has_t1 = (qi0 + 1) < p.nT;
-      const int kvl = effective_kv_len(p.kv_len, b, p.N);
-      int kpre = 0;   // K loads of this item issued during its set-up (producer thread)
-      // Q first, then the union list of live key tiles of the two Q tiles
-      // (ascending j), then the K tiles of the first ring's worth of entries:
-      // their loads overlap the rest of the set-up
+      const int kvl = effective_kv_len(p.kv_len, bh / p.H, p.N);
+      uint16_t* lst = list + qb * kListMax;
       if (lane == 0) {
-        if (kq == 0u) {
-          tma_prefetch_map(&tq);
-          tma_prefetch_map(&tk);
-        }
         const uint32_t qbytes = (has_t1 ? 2u : 1u) * L::kTileBytes;
-        mbar_arrive_expect_tx(bar(L::bQFull), qbytes);
+        mbar_arrive_expect_tx(bar(L::bQFull + qb), qbytes);
         for (int t = 0; t < (has_t1 ? 2 : 1); ++t)
           for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sbase + L::kQ + t * L::kTileBytes + h * 16384, &tq, bar(L::bQFull), 64 * h,
-                        kTile * (qi0 + t), bh);
+            tma_load_3d(sbase + L::kQ + (2 * qb + t) * L::kTileBytes + h * 16384, &tq, bar(L::bQFull + qb),
+                        64 * h, kTile * (qi0 + t), bh);
+        ++nq[qb];
       }
       int count = 0;
       int last[2] = {-1, -1};
-      for (int base = 0; base < p.nT; base += 32) {
-        const int j = base + lane;
+      for (int jb = 0; jb < p.nT; jb += 32) {
+        const int j = jb + lane;
         uint32_t e = 0;
         if (j < p.nT) {
           const int s0 = tile_state(qi0, j, kvl, p.nT, p.causal, p.block_mask);
@@ -218,7 +225,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
         const bool live = (e >> 10) & 3u;
         const uint32_t ball = __ballot_sync(0xFFFFFFFFu, live);
-        if (live) list[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
+        if (live) lst[count + __popc(ball & ((1u << lane) - 1u))] = (uint16_t)e;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {   // list index of the last entry live for Q tile t so far
           const uint32_t bt = __ballot_sync(0xFFFFFFFFu, (e >> (10 + t)) & 1u);
@@ -227,29 +234,42 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         count += __popc(ball);
       }
       __syncwarp();
+      int kpre = 0;
       if (lane == 0) {
-        misc[2] = (uint32_t)count;
-        misc[4] = (uint32_t)last[0];
-        misc[5] = (uint32_t)last[1];
-        // K of the first ring's worth of entries: their loads overlap the rest
-        // of the set-up (the slots' previous users are complete: the previous
-        // item ended with all its products read out)
+        misc[8 + 4 * qb] = (uint32_t)count;
+        misc[9 + 4 * qb] = (uint32_t)last[0];
+        misc[10 + 4 * qb] = (uint32_t)last[1];
+        // (a slot's previous user is an entry of this or an earlier item whose
+        // S products free it)
         for (; kpre < count && kpre < L::kStagesK; ++kpre) {
           if (p.chk.stall != 0u && kpre >= 1) break;   // test of the timeout path: K of entry 1 never comes
-          const int n = eK + kpre;
+          const int n = base + kpre;
           const int sk = n % L::kStagesK;
           if (n >= L::kStagesK && !mbar_wait(bar(L::bKEmpty + sk), (uint32_t)(n / L::kStagesK - 1) & 1u, ctl, 1))
             break;
           mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk), 64 * h,
-                        kTile * entry_j(list[kpre]), bh);
+                        kTile * entry_j(lst[kpre]), bh);
           ++nk;
         }
       }
+      return kpre;
+    };
+    if (lane == 0) {
+      tma_prefetch_map(&tq);
+      tma_prefetch_map(&tk);
+    }
+    int kpre = setup(item, 0, 0);   // K loads of the current item issued during its set-up (lane 0)
+    for (;; ++kq) {
+      const int qb = (int)(kq % L::kQBuf);
+      int bh = 0;
+      (void)split_grouped(item, p.group, nC, BH, &bh);
       item_sync();
-      const int len = (int)misc[2];
+      const int len = (int)misc[8 + 4 * qb];
+      const uint16_t* lst = list + qb * kListMax;
       // ------------------------------------------------------------ Q and K producer
+      int next = -1;
       if (lane == 0) {
         // K of ring entry eK + e into slot (eK + e) mod S, once the MMAs of the
         // entry that used the slot before (of this item or an earlier one)
@@ -264,12 +284,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           mbar_arrive_expect_tx(bar(L::bKFull + sk), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sbase + L::kK + sk * L::kTileBytes + h * 16384, &tk, bar(L::bKFull + sk),
-                        64 * h, kTile * entry_j(list[e]), bh);
+                        64 * h, kTile * entry_j(lst[e]), bh);
           ++nk;
         }
         // every K load of the item is issued: ask for the next item (the answer
         // lands while this one is computed)
-        int next = -1;
         if (ok) {
           mbar_arrive_expect_tx(bar(L::bClc), 16u);
           clc_try_cancel(sbase + L::kClc, bar(L::bClc));
@@ -285,16 +304,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
         misc[6] = (uint32_t)next;
       }
+      // with two buffers the next item is set up while this one runs (the
+      // other buffer's item has been stored and its list read: every role
+      // has passed the barrier after it)
+      next = __shfl_sync(0xFFFFFFFFu, next, 0);
+      if (L::kQBuf == 2 && next >= 0) kpre = setup(next, qb ^ 1, eK + len);
       item_sync();
       item = next_item();
       if (item < 0) break;
       eK += len;
+      if (L::kQBuf == 1) kpre = setup(item, 0, eK);
     }
     // every load and cancellation request issued has completed before the
     // CTA exits; loads were issued in ring order, so the last load into slot
     // s was number s + S * floor((n - 1 - s) / S)
     if (lane == 0) {
-      drain_wait(bar(L::bQFull), kq & 1u);
+      for (int b = 0; b < L::kQBuf; ++b)
+        if (nq[b] > 0u) drain_wait(bar(L::bQFull + b), (nq[b] - 1u) & 1u);
       for (int s = 0; s < L::kStagesK && s < nk; ++s)
         drain_wait(bar(L::bKFull + s), (uint32_t)((nk - 1 - s) / L::kStagesK) & 1u);
       if (clc_out) drain_wait(bar(L::bClc), kq & 1u);
@@ -302,10 +328,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   } else if (warp == 10) {
     regs_dec<kOtherRegs>();
     for (;; ++kq) {
+      const int qb = (int)(kq % L::kQBuf);
       int bh = 0;
       (void)split_grouped(item, p.group, nC, BH, &bh);
       item_sync();
-      const int len = (int)misc[2];
+      const int len = (int)misc[8 + 4 * qb];
+      const uint16_t* lst = list + qb * kListMax;
       // ------------------------------------------------------------ V producer
       // (its own thread, so that the K ring can run ahead of the V ring)
       if (lane == 0) {
@@ -318,7 +346,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           mbar_arrive_expect_tx(bar(L::bVFull + sv), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sbase + L::kV + sv * L::kTileBytes + h * 16384, &tv, bar(L::bVFull + sv),
-                        64 * h, kTile * entry_j(list[e]), bh);
+                        64 * h, kTile * entry_j(lst[e]), bh);
           ++nv;
         }
       }
@@ -333,8 +361,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
   } else if (warp == 9) {
     regs_dec<kOtherRegs>();
     for (;; ++kq) {
+      const int qb = (int)(kq % L::kQBuf);
       item_sync();
-      const int len = (int)misc[2];
+      const int len = (int)misc[8 + 4 * qb];
+      const uint16_t* lst = list + qb * kListMax;
       // ------------------------------------------------------------ MMA issuer
       // Fixed schedule over the union list: at entry e, for each Q tile t, first
       // the pending O_t += P_t V of t's previous live entry (waiting for P_t),
@@ -351,16 +381,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
         // P_t: over S_t, or in columns of its own (after O_1)
         const uint32_t tP[2] = {L::kOwnP ? tmem + 256u + 2u * D : tS[0], L::kOwnP ? tmem + 320u + 2u * D : tS[1]};
-        const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ, 0), desc_kmajor(sbase + L::kQ + L::kTileBytes, 0)};
+        const uint64_t dQ[2] = {desc_kmajor(sbase + L::kQ + 2 * qb * L::kTileBytes, 0),
+                                desc_kmajor(sbase + L::kQ + (2 * qb + 1) * L::kTileBytes, 0)};
         const uint64_t dK0 = desc_kmajor(sbase + L::kK, 0);
         const uint64_t dV0 = desc_mnmajor(sbase + L::kV, 0);
         constexpr uint64_t kSlotStep = (uint64_t)(L::kTileBytes >> 4);
         int prev[2] = {-1, -1};       // entry of the pending PV of each Q tile
         // the last entry live for each Q tile: its PV completes O_t, which the
         // softmax group may then read out while the other tile's products run
-        const int lastE[2] = {(int)misc[4], (int)misc[5]};
+        const int lastE[2] = {(int)misc[9 + 4 * qb], (int)misc[10 + 4 * qb]};
         uint32_t npv_item[2] = {0u, 0u};   // PV groups of this item per Q tile
-        bool ok = mbar_wait_warp(bar(L::bQFull), kq & 1u, ctl, 4);
+        bool ok = mbar_wait_warp(bar(L::bQFull + qb), (kq / L::kQBuf) & 1u, ctl, 4);
         tc_fence_after();
 
         // O_t += P_t V_{entry pe}
@@ -389,7 +420,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           //   S0(e), S1(e), PV0(e-1), PV1(e-1), S0(e+1), ...
           // so S_t(e+1) is computed while group t still works on S_t(e).
           for (int e = 0; e < len && ok; ++e) {
-            const uint32_t ent = list[e];
+            const uint32_t ent = lst[e];
             const int sk = (eK + e) % L::kStagesK;
             bool k_ready = false;
 #pragma unroll
@@ -421,7 +452,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           }
         } else {
           for (int e = 0; e < len && ok; ++e) {
-            const uint32_t ent = list[e];
+            const uint32_t ent = lst[e];
             const int sk = (eK + e) % L::kStagesK;
             bool k_ready = false;
 #pragma unroll
@@ -478,7 +509,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       const int qi0 = 2 * c;
       const int kvl = effective_kv_len(p.kv_len, bh / p.H, p.N);
       item_sync();
-      const int len = (int)misc[2];
+      const int qb = (int)(kq % L::kQBuf);
+      const int len = (int)misc[8 + 4 * qb];
+      const uint16_t* lst = list + qb * kListMax;
       // ------------------------------------------------------------ softmax groups
       const int t = warp >> 2;                 // Q tile of this warpgroup
       const int r = tid & 127;                 // row within the tile = TMEM lane
@@ -495,7 +528,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
       uint32_t n = 0;   // S tiles of this item (nS: of all items)
       bool ok = (qi < p.nT);
       for (int e = 0; e < len && ok; ++e) {
-        const uint32_t ent = list[e];
+        const uint32_t ent = lst[e];
         if (!entry_live(ent, t)) continue;
         // dropout: keep bits of this row for the entry's 128 keys, made before S
         // is awaited, so that the generator runs while the tensor pipe computes
@@ -663,12 +696,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         // all MMAs that read Q_t have completed (or never ran); make sure the
         // Q load itself has landed before its buffer is reused for staging O
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (ok) ok = mbar_wait_warp(bar(L::bQFull), kq & 1u, ctl, 12 + t);
+        if (ok) ok = mbar_wait_warp(bar(L::bQFull + qb), (kq / L::kQBuf) & 1u, ctl, 12 + t);
         if (ok && n > 0) ok = mbar_wait_warp(bar(L::bOFinal + t), nOF & 1u, ctl, 14 + t);
         if (n > 0) ++nOF;
-        if (!ok) drain_wait(bar(L::bQFull), kq & 1u);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
+        if (!ok) drain_wait(bar(L::bQFull + qb), (kq / L::kQBuf) & 1u);   // after an abort: the Q load (always issued) lands before its buffer is rewritten
         tc_fence_after();
-        uint8_t* stage = smem + L::kQ + t * L::kTileBytes;
+        uint8_t* stage = smem + L::kQ + (2 * qb + t) * L::kTileBytes;
         const float inv_l = (n > 0 && l > 0.f) ? (DROP ? p.drop.keep_scale : 1.f) / l : 0.f;
         const bool have_o = ok && n > 0;
 #pragma unroll
