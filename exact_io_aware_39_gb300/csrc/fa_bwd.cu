@@ -560,10 +560,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           x[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], sl2, -l.w));
         }
         if (partial) {
-          const int q0 = kTile * i + cb;
+          // key row krow is masked for query q0 + c when it lies past the
+          // query (causal: c < krow - q0) or at or past the key length (every c)
+          const int lim = krow >= w.kvl ? kC : (p.causal ? krow - (kTile * i + cb) : 0);
 #pragma unroll
           for (int c = 0; c < kC; ++c)
-            if ((p.causal && krow > q0 + c) || krow >= w.kvl) x[c] = 0.f;
+            if (c < lim) x[c] = 0.f;
         }
         auto kept = [&](int c) -> bool {
           const int j = (c >> 2) & 3, d = c & 3;

@@ -589,12 +589,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           mbar_arrive_warp(bar(L::bSFree + t));
         }
         if (entry_partial(ent, t)) {
-          const int key0 = kTile * entry_j(ent);
+          // a key is masked when it lies past the row (causal) or at or past the
+          // key length: key >= min(row + 1, key length), i.e. column i >= lim
+          const int lim = (p.causal ? min(row + 1, kvl) : kvl) - kTile * entry_j(ent);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const int key = key0 + i;
-            if ((p.causal && key > row) || key >= kvl) x[i] = -INFINITY;
-          }
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) x[i] = -INFINITY;
         }
         if (L::kOwnP && nS > 0) {
           // the previous O_t += P_t V has completed (of this item or the last
