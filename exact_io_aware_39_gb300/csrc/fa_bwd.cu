@@ -602,11 +602,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = mbar_wait_warp(bar(L::bdPFull), (uint32_t)g & 1u, ctl, 122))) break;
         if (g > 0 && !(ok = mbar_wait_warp(bar(L::bdSEmpty), (uint32_t)(g - 1) & 1u, ctl, 123))) break;
         tc_fence_after();
+        // at d = 128 both 32-column halves of this warpgroup's dP^T are loaded
+        // before the first wait, so their TMEM latencies overlap (measured:
+        // +0.9 % on the backward at d = 128; at d = 64 the 32 extra live
+        // registers spill and it lost 3.5 %)
+        constexpr bool kBothHalves = (D == 128);
+        uint32_t ud[kC / 32][32];
+        if constexpr (kBothHalves) {
+#pragma unroll
+          for (int cc = 0; cc < kC / 32; ++cc) tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, ud[cc]);
+#pragma unroll
+          for (int cc = 0; cc < kC / 32; ++cc) tmem_ld_wait(ud[cc]);
+        }
 #pragma unroll
         for (int cc = 0; cc < kC / 32; ++cc) {
-          uint32_t u[32];
-          tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, u);
-          tmem_ld_wait(u);
+          if constexpr (!kBothHalves) {
+            tmem_ld32(tP + lane_off + (uint32_t)cb + 32u * cc, ud[cc]);
+            tmem_ld_wait(ud[cc]);
+          }
+          const uint32_t* u = ud[cc];
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
