@@ -416,11 +416,21 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // before the rest (2, 3 and 6, 7), so half of dK runs while dS is
           // finished (measured: +1.5 % at d = 128, -0.4 to -1.2 % at d = 64)
           const uint64_t mQ = desc_mnmajor(sQ, 0);
+          // dQ_i = dS K: with dS^T handed over in halves, dQ goes right after
+          // dS is complete, in front of the second half of dK, so that its
+          // drain overlaps that half
+          auto issue_dq = [&]() {
+#pragma unroll
+            for (int ks = 0; ks < kTile / 16; ++ks)
+              mma_ss_t<kW>(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
+            mma_commit_t<kW>(bar(L::bdQFull));
+          };
 #pragma unroll
           for (int half = kSplitDS ? 0 : 1; half < 2; ++half) {
             if (!(ok = mbar_wait_t<kW>(bar(half == 0 ? L::bdSHalf : L::bdSFull), (uint32_t)g & 1u, ctl, 115)))
               break;
             tc_fence_after();
+            if (kSplitDS && half == 1) issue_dq();
 #pragma unroll
             for (int k4 = 0; k4 < (kSplitDS ? 4 : 8); ++k4) {
               const int ks = kSplitDS ? 2 * half + (k4 & 1) + 4 * (k4 >> 1) : k4;
@@ -430,13 +440,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           }
           if (!ok) break;
           mma_commit_t<kW>(bar(L::bQEmpty + s));   // the slot's Q has been read for the last time
-          // at d = 64 the previous dQ partial must have been read out of its columns
-          if (kOwnDQ && g > 0 && !(ok = mbar_wait_t<kW>(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ss_t<kW>(tQ, desc_mnmajor(sdS, ks), mK + mnmajor_step(ks), idQ, ks > 0 ? 1u : 0u);
-          mma_commit_t<kW>(bar(L::bdQFull));
+          if (!kSplitDS) {
+            // at d = 64 the previous dQ partial must have been read out of its columns
+            if (kOwnDQ && g > 0 && !(ok = mbar_wait_t<kW>(bar(L::bdQFree), (uint32_t)(g - 1) & 1u, ctl, 112))) break;
+            tc_fence_after();
+            issue_dq();
+          }
           mma_commit_t<kW>(bar(L::bdSEmpty));      // dK and dQ have read dS
           if (!kEarlyS && inext < p.nT && !(ok = issue_s(sK, g + 1))) break;
           i = inext;
