@@ -27,22 +27,27 @@
 //        dV  += P^T dO         (A = P^T from TMEM, B = dO MN-major)
 //        dK  += dS^T Q         (A = dS^T from TMEM, B = Q MN-major)
 //        dQ_i = dS K           (A = the same dS^T buffer read MN-major, B = K MN-major)
-//      At d = 128, S^T of the next query tile is issued after dK and dQ of
-//      the current one, which leaves its Q load the longest window (the dQ
-//      partial reuses the dP^T columns, so the next dP^T waits for its drain;
-//      S^T runs meanwhile). At d = 64 the dQ partial has TMEM columns of its
-//      own and S^T of the next tile follows dV directly, so that P of the
-//      next tile is recomputed while dK, dQ and the next dP^T run.
+//      At d = 128 without dropout, dQ is issued as soon as dS is complete,
+//      between the two halves of dK, and S^T of the next query tile after dK,
+//      which leaves its Q load the longest window (the dQ partial reuses the
+//      dP^T columns, so the next dP^T waits for its drain; S^T runs
+//      meanwhile). At d = 64 the dQ partial has TMEM columns of its own and
+//      S^T of the next tile follows dV directly, so that P of the next tile
+//      is recomputed while dK, dQ and the next dP^T run; with dropout the
+//      same early S^T is used at d = 128 too (dS^T then packed over the
+//      consumed dP^T columns).
 //      Each dQ partial is drained from TMEM into shared memory (the dO ring
 //      slot of its own query tile, dead once dQ is issued, in two rounds) and
 //      added into the fp32 workspace with TMA reduce-add, so L2 receives whole
 //      128-byte lines. Q and the row statistics have their own barrier and are
 //      refilled as soon as dK has read Q; dO only after the reductions have
 //      read the slot.
-//      Warps: 0-3 and 4-7 recompute P and dS for query columns 0-63 and
-//      64-127 (thread = key row), 8-11 drain dQ from TMEM into the workspace
-//      (thread = query row), 12 TMA producer, 13 MMA, 14-15 idle (their
-//      warpgroup hands its registers to the others).
+//      Warps (BwdWarps): without dropout 0-3 and 4-7 recompute P and dS for
+//      query columns 0-63 and 64-127 (thread = key row), 8-11 drain dQ from
+//      TMEM into the workspace (thread = query row), 12 TMA producer, 13 MMA,
+//      14-15 idle (their warpgroup hands its registers to the others); with
+//      dropout four P/dS warpgroups of 32 query columns (warps 0-15), then
+//      the drain (16-19), the producer (20), MMA (21) and two idle warps.
 //   3. fa_bwd_dq:   dQ = bf16(scale * dQ_acc).
 #include "fa_common.cuh"
 #include "fa_ptx.cuh"
