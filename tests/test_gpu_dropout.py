@@ -129,6 +129,43 @@ def test_dropout_masks_bit_exact(fa, p, seed):
         assert np.array_equal(got_t, keep[:128, :].T.astype(np.int64)), f"backward mask differs for head {h}"
 
 
+@pytest.mark.parametrize("p,seed", [(0.3, 23), (0.6, (3 << 32) | 5)])
+def test_dropout_masks_bit_exact_d64(fa, p, seed):
+    """The same at d = 64 (the 64-column kernels: their forward, and the
+    backward's four P/dS warpgroups of 32 queries). With 64 value columns
+    V_j = w_j e_(j mod 64) carries four keys per column, w = 1, 2, 4, 8 for
+    keys 0-63, 64-127, 128-191, 192-255, so O[i, c] = (Z[i, c] + 2 Z[i, c + 64]
+    + 4 Z[i, c + 128] + 8 Z[i, c + 192]) s / N, a 4-bit code. In the backward
+    pass dO = I on queries 64 m .. 64 m + 63 gives dV[j, c] = Z[64 m + c, j] s / N;
+    two calls cover the first query tile."""
+    B, H, N, d = 1, 2, 256, 64
+    dev = torch.device("cuda:0")
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device=dev)
+    k = torch.randn(B, H, N, d, dtype=torch.bfloat16, device=dev)
+    eye = torch.eye(64)
+    v = torch.cat([eye, 2 * eye, 4 * eye, 8 * eye], 0).to(torch.bfloat16)[None, None].repeat(B, H, 1, 1).to(dev)
+    o, lse = fa.attention_fwd(q, k, v, 1.0, False, p_drop=p, seed=seed)
+    dvs = []
+    for m in range(2):
+        do = torch.zeros(N, d)
+        do[64 * m:64 * m + 64] = eye
+        do = do.to(torch.bfloat16)[None, None].repeat(B, H, 1, 1).to(dev)
+        dvs.append(fa.attention_bwd(q, k, v, o, do, lse, 1.0, False, p_drop=p, seed=seed)[2])
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    t, s = oracle.threshold(p)
+    unit = s / N
+    for h in range(H):
+        keep, _ = oracle.keep_mask(seed, h, N, p)
+        keep = keep.astype(np.int64)
+        code = np.rint(o[0, h].float().cpu().numpy() / unit).astype(np.int64)     # [N, 64]
+        want = keep[:, :64] + 2 * keep[:, 64:128] + 4 * keep[:, 128:192] + 8 * keep[:, 192:]
+        assert np.array_equal(code, want), f"forward mask differs for head {h}"
+        for m in range(2):
+            got_t = np.rint(dvs[m][0, h].float().cpu().numpy() / unit).astype(np.int64)   # [keys, 64 queries]
+            assert np.array_equal(got_t, keep[64 * m:64 * m + 64, :].T), f"backward mask differs for head {h}, queries {64 * m}+"
+
+
 def test_dropout_probability_validated(fa):
     dev = torch.device("cuda:0")
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device=dev)
