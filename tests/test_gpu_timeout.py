@@ -83,3 +83,32 @@ def test_backward_wait_runs_out_and_device_stays_usable(fa, d, causal):
     # dQ partials are added in arrival order: the same values within rounding
     assert torch.equal(_bits(dk1), _bits(dk0)) and torch.equal(_bits(dv1), _bits(dv0))
     assert torch.allclose(dq1.float(), dq0.float(), rtol=1e-2, atol=1e-3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_dropout_kernels_wait_runs_out_and_device_stays_usable(fa, d):
+    """The dropout instances run other warp layouts (the backward's four P/dS
+    warpgroups, which at d = 64 agree across all sixteen compute warps): the
+    same stalled loader ends both kernels with a timeout, and the next calls
+    give the bits of a fresh run."""
+    w, (q, k, v, do) = _inputs(d, True)
+    kw = dict(p_drop=0.2, seed=77)
+    o0, l0 = fa.attention_fwd(q, k, v, w.scale, True, **kw)
+    dq0, dk0, dv0 = fa.attention_bwd(q, k, v, o0, do, l0, w.scale, True, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    fa.attention_fwd(q, k, v, w.scale, True, wait_limit_us=LIMIT_US, test_stall=1, **kw)
+    torch.cuda.synchronize()
+    st, detail = fa.device_error()
+    assert st == FA_ERR_DEVICE_TIMEOUT and detail[1] < 100, detail
+    fa.attention_bwd(q, k, v, o0, do, l0, w.scale, True, wait_limit_us=LIMIT_US, test_stall=1, **kw)
+    torch.cuda.synchronize()
+    st, detail = fa.device_error()
+    assert st == FA_ERR_DEVICE_TIMEOUT and 100 <= detail[1] < 200, detail
+    o1, l1 = fa.attention_fwd(q, k, v, w.scale, True, **kw)
+    dq1, dk1, dv1 = fa.attention_bwd(q, k, v, o1, do, l1, w.scale, True, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_error()[0] == 0
+    assert torch.equal(_bits(o1), _bits(o0)) and torch.equal(_bits(l1), _bits(l0))
+    assert torch.equal(_bits(dk1), _bits(dk0)) and torch.equal(_bits(dv1), _bits(dv0))
+
