@@ -279,7 +279,7 @@ def test_tile_map_bit_exact(fa, spec):
     assert np.array_equal(got, want)
 
 
-def _recorded_tiles(fa, c):
+def _recorded_tiles(fa, c, p_drop=0.0):
     """The tiles the forward and the backward kernels computed, as recorded
     through fa_options.tile_record: two uint8 arrays [B, H, nT, nT]."""
     dev = torch.device("cuda:0")
@@ -290,8 +290,9 @@ def _recorded_tiles(fa, c):
     nT = (N + 127) // 128
     rec_f = torch.zeros((B, H, nT, nT), dtype=torch.uint8, device=dev)
     rec_b = torch.zeros_like(rec_f)
-    o, lse = fa.attention_fwd(q, k, v, c["scale"], c["causal"], kv, bm, tile_record=rec_f)
-    fa.attention_bwd(q, k, v, o, do, lse, c["scale"], c["causal"], kv, bm, tile_record=rec_b)
+    kw = dict(p_drop=p_drop, seed=5) if p_drop > 0 else {}
+    o, lse = fa.attention_fwd(q, k, v, c["scale"], c["causal"], kv, bm, tile_record=rec_f, **kw)
+    fa.attention_bwd(q, k, v, o, do, lse, c["scale"], c["causal"], kv, bm, tile_record=rec_b, **kw)
     torch.cuda.synchronize()
     assert fa.device_error()[0] == 0
     return rec_f.cpu().numpy(), rec_b.cpu().numpy()
@@ -307,6 +308,18 @@ def test_kernels_compute_exactly_the_classified_tiles(fa, spec):
     computed twice would all differ."""
     c = _small_case(*spec)
     rec_f, rec_b = _recorded_tiles(fa, c)
+    want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
+    want = np.broadcast_to(want[:, None], rec_f.shape)
+    assert np.array_equal(rec_f, want)
+    assert np.array_equal(rec_b, want)
+
+
+@pytest.mark.parametrize("spec", [s for s in SMALL if s[4] <= 128], ids=[s[0] for s in SMALL if s[4] <= 128])
+def test_dropout_kernels_compute_exactly_the_classified_tiles(fa, spec):
+    """The same record from the dropout instances (other warp layouts in the
+    backward: four P/dS warpgroups)."""
+    c = _small_case(*spec)
+    rec_f, rec_b = _recorded_tiles(fa, c, p_drop=0.2)
     want = oracle.tile_states(c["B"], c["N"], c["causal"], c["kv_len"], c["block_mask"])
     want = np.broadcast_to(want[:, None], rec_f.shape)
     assert np.array_equal(rec_f, want)
