@@ -37,7 +37,10 @@
 //     pair;
 //   * the running max is moved (and O rescaled) only when a new row max
 //     exceeds it by more than 2^8; the final O / l and LSE use the same
-//     reference max, so the result is unchanged.
+//     reference max, so the result is unchanged;
+//   * with P over S (d = 128), P of a tile's first 64 keys goes to the
+//     tensor core before the rest is formed, so half of P V overlaps the
+//     second half of the exponentials.
 #include "fa_common.cuh"
 #include "fa_ptx.cuh"
 
@@ -88,7 +91,8 @@ struct FwdLayout {
   static constexpr int bOFinal = bPFull + 2;          // [2]
   static constexpr int bSFree = bOFinal + 2;          // [2] S_t read into registers (own P columns only)
   static constexpr int bPVDone = bSFree + 2;          // [2] O_t += P_t V complete (own P columns only)
-  static constexpr int bClc = bPVDone + 2;            // the next item's cancellation answer has arrived
+  static constexpr int bPHalf = bPVDone + 2;          // [2] P_t of the first 64 keys is in TMEM (P over S only)
+  static constexpr int bClc = bPHalf + 2;             // the next item's cancellation answer has arrived
   static constexpr int bDrain = bClc + 1;
   static constexpr int kNumBars = bDrain + 1;
   // 32-bit words: tmem slot, abort flag, -, wait limit, -, -, next item, -;
@@ -113,6 +117,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
               const FwdParams p) {
   using L = FwdLayout<D>;
+  // With P over S (d = 128) and without dropout, P of a tile's first 64 keys
+  // goes to the tensor core before the rest is formed, and its half of P V
+  // runs meanwhile; the softmax then always takes the row max first, since P
+  // may not be formed again once half of it has been used (measured: forward
+  // long_causal 1729 -> 1817 TFLOP/s; with dropout -1.7 %, not used there)
+  constexpr bool kHalfP = !L::kOwnP && !DROP;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
 
@@ -140,7 +150,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
   if (tid == 0) {
     for (int i = 0; i < L::kNumBars; ++i)
-      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1 || i == L::bSFree || i == L::bSFree + 1) ? 4u
+      mbar_init(bar(i), (i == L::bPFull || i == L::bPFull + 1 || i == L::bSFree || i == L::bSFree + 1 ||
+                         i == L::bPHalf || i == L::bPHalf + 1) ? 4u
                                                                                                       : 1u);   // 4 = warps
     abort_flag[0] = 0u;
     abort_flag[2] = p.chk.wait_us;   // the wait limit, read by the slow path of every wait
@@ -398,14 +409,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         auto issue_pv = [&](int t, int pe) -> bool {
           const int nvp = eV + pe;
           const int sv = nvp % L::kStagesV;
-          if (!mbar_wait_warp(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
+          if (!mbar_wait_warp(bar((kHalfP ? L::bPHalf : L::bPFull) + t), npv[t] & 1u, ctl, 5)) return false;
           if (!mbar_wait_warp(bar(L::bVFull + sv), (uint32_t)(nvp / L::kStagesV) & 1u, ctl, 6)) return false;
           tc_fence_after();
           const uint64_t dV = dV0 + (uint64_t)sv * kSlotStep;
           const uint32_t acc0 = npv_item[t] > 0 ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
+          for (int ks = 0; ks < kTile / 16; ++ks) {
+            if (kHalfP && ks == kTile / 32) {   // the second half of P
+              if (!mbar_wait_warp(bar(L::bPFull + t), npv[t] & 1u, ctl, 5)) return false;
+              tc_fence_after();
+            }
             mma_ts_w(tO[t], tP[t] + (uint32_t)ks * 8u, dV + mnmajor_step(ks), idO, ks > 0 ? 1u : acc0);
+          }
           if constexpr (L::kOwnP) mma_commit_w(bar(L::bPVDone + t));   // P_t may be rewritten, O_t rescaled
           if (pe == lastE[t]) mma_commit_w(bar(L::bOFinal + t));       // O_t is complete
           ++npv[t];
@@ -602,7 +618,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
           if (!mbar_wait_warp(bar(L::bPVDone + t), (nS - 1u) & 1u, ctl, 16 + t)) { ok = false; break; }
           tc_fence_after();
         }
-        // Two passes at most. Pass 0 (not for a row block's first tile) takes the
+        // Two passes at most (at d = 64 without dropout; otherwise only pass 1).
+        // Pass 0 (not for a row block's first tile) takes the
         // exponentials with the current reference max: if every row of the warp
         // then sums to less than 2^8, no score exceeds the reference by the
         // rescale threshold, so the row max would not have moved it and P is
@@ -611,7 +628,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         // and redoes the exponentials (the whole warp: the TMEM stores are
         // warp-collective). This saves the row max on most tiles.
         float s_row = 0.f;
-        for (int pass = (n == 0 || DROP) ? 1 : 0; pass < 2; ++pass) {   // (with dropout: always the row max)
+        // (with dropout, and when half of P goes ahead: always the row max)
+        for (int pass = (n == 0 || DROP || kHalfP) ? 1 : 0; pass < 2; ++pass) {
           if (pass == 1) {
             // row max with three-input max: 8 independent chains over 128 scores
             float mx8[8];
@@ -676,6 +694,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
               }
             }
             tmem_st32(tP + 32u * hh, pk);
+            if (kHalfP && hh == 0) {   // the first 64 keys' P: its half of P V may start
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive_warp(bar(L::bPHalf + t));
+            }
           }
           tmem_st_wait();
           const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
